@@ -1,0 +1,266 @@
+/*
+ * opw.h -- C ABI of the tile-centric AllGather->GEMM / GEMM->ReduceScatter
+ * overlap library for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow "Triton-distributed Semantics" (sections
+ * "Producer-Consumer Model", "Signal-Based Synchronization", "Symmetric
+ * Memory Model", "AllGather and GEMM Overlapping", "GEMM and ReduceScatter
+ * Overlapping", "Threadblock Swizzling", "Token-Based Data Dependency") and
+ * "Distributed Architecture Design" (section 2.3 SignalOp, section 5 symmetric
+ * heap, section 6 signal/wait mechanisms).  The epoch carried by every signal
+ * follows the put_signal / wait_signal(flag, epoch) contract of the Aboleth
+ * README ("Tier 1" device library).
+ *
+ * All R ranks are LOGICAL ranks on one GPU: each rank owns one slice of a
+ * single device allocation (the "heap"), and an offset table stands in for
+ * the peer mappings of a real symmetric heap.
+ *
+ * Conventions
+ *   - Pointers named *_dev are device pointers; everything else is host.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *   - Matrices are row-major bf16 (IEEE binary32 upper half), element
+ *     (i, j) of an [rows, cols] matrix at byte offset 2*(i*cols + j).
+ *   - Every call that takes a stream is asynchronous: argument errors are
+ *     returned at once; errors found on the device (a wait that timed out, a
+ *     flag protocol violation) are latched in the signal object's status
+ *     word and returned by opw_status_sync().  Once a device error is
+ *     latched, later launches on that signal object do no work until
+ *     opw_signal_reset().
+ *   - No function throws, prints or aborts.  No function allocates memory
+ *     except opw_signal_alloc().
+ *   - The caller owns every buffer it passes and keeps it alive until the
+ *     stream has executed the call.  The library owns only opw_signal.
+ */
+#ifndef OPW_H
+#define OPW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define OPW_ABI_VERSION 1
+#define OPW_MAX_RANKS 8
+
+/* ---------------------------------------------------------------- status */
+
+typedef int32_t opw_status;
+#define OPW_OK                    0
+#define OPW_ERR_INVALID_ARG       1  /* NULL pointer, bad enum, R out of range, too few slots */
+#define OPW_ERR_UNSUPPORTED_SHAPE 2  /* a size is not a multiple of the flag tile, or <= 0 */
+#define OPW_ERR_MISALIGNED        3  /* a pointer or offset is not 16-byte aligned (TMA rule) */
+#define OPW_ERR_BAD_EPOCH         4  /* epoch is not the next one for this signal object */
+#define OPW_ERR_CUDA              5  /* a CUDA runtime/driver call failed */
+#define OPW_ERR_TIMEOUT           6  /* a device-side wait ran past opts.timeout_ns */
+#define OPW_ERR_FLAG_PROTOCOL     7  /* a flag held a value other than the epoch it should */
+#define OPW_ERR_NOT_READY         8  /* the signal object has a latched device error; reset it */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* opw_status_str(opw_status s);
+
+/* OPW_ABI_VERSION of the loaded library. */
+int32_t opw_abi_version(void);
+
+/* ---------------------------------------------------------------- signals */
+
+/*
+ * A signal object: an array of int64 flags in device memory ("Signal-Based
+ * Synchronization": one signal per tile), the host-side epoch counter, and a
+ * device status word.  A flag holds the last epoch published for its tile
+ * (SignalOp SET, "Distributed Architecture Design" 2.3); a waiter spins until
+ * flag >= epoch (the GE predicate of section 6.3).  Waiting never modifies a
+ * flag (non-consuming wait, section 6.3); only opw_signal_reset() writes
+ * flags back to 0 ("the constraint falls on the reset side").  Flags are
+ * dense (8 bytes apart): on GB300 the L2 is the coherence point for
+ * .gpu-scope release/acquire, so the 64-byte slot stride that section 4.2
+ * needs on Ascend buys nothing here.
+ */
+typedef struct opw_signal opw_signal;
+
+/*
+ * Allocate a signal object with `num_slots` flags (>= 1), all 0, epoch 0.
+ * The zeroing is enqueued on `stream`.  On success *out owns device memory
+ * until opw_signal_free().  Errors: INVALID_ARG (out NULL, num_slots < 1),
+ * CUDA (allocation failed; *out is left NULL).
+ */
+opw_status opw_signal_alloc(opw_signal** out, int64_t num_slots, void* stream);
+
+/*
+ * Enqueue on `stream`: every flag := 0, the device status word := OK, the
+ * internal counters := 0; and set the host epoch counter to 0, so the next
+ * epoch is 1.  The caller must not have launches on this object in flight
+ * on other streams.  Errors: INVALID_ARG (NULL), CUDA.
+ */
+opw_status opw_signal_reset(opw_signal* sig, void* stream);
+
+/* Free a signal object (synchronises the device first).  NULL is a no-op. */
+opw_status opw_signal_free(opw_signal* sig);
+
+/* *epoch := last epoch published on this object + 1 (the value the next
+ * fused or producer-only launch must pass).  Errors: INVALID_ARG. */
+opw_status opw_signal_next_epoch(const opw_signal* sig, uint64_t* epoch);
+
+/* Device pointer to the flag array and its length (for read-back checks).
+ * Errors: INVALID_ARG. */
+opw_status opw_signal_flags(const opw_signal* sig, int64_t** flags_dev, int64_t* num_slots);
+
+/*
+ * Synchronise `stream`, then read and return the device status word.  If a
+ * device-side error was latched, *rank / *tile (either may be NULL) receive
+ * the logical rank and flag slot the failing wait was on (-1 if none).
+ * The latched error stays until opw_signal_reset().
+ */
+opw_status opw_status_sync(opw_signal* sig, void* stream, int32_t* rank, int32_t* tile);
+
+/* ---------------------------------------------------------------- heap */
+
+/*
+ * Logical symmetric heap ("Distributed Architecture Design" 5.3): rank r's
+ * slice starts at heap_dev + rank_off[r].  A symmetric object at offset `off`
+ * is at heap_dev + rank_off[r] + off on rank r, which is symm_at(ptr, r) =
+ * ptr - heap_base[self] + heap_base[r] with heap_base[r] = heap_dev +
+ * rank_off[r].  rank_off is a HOST array of R entries, read during the call
+ * only; entries need not be increasing (a permuted table is allowed) and
+ * must be multiples of 16.
+ */
+typedef struct {
+    void* heap_dev;
+    const int64_t* rank_off;
+    int32_t R;          /* 1 .. OPW_MAX_RANKS */
+    int32_t reserved;   /* must be 0 */
+} opw_symm;
+
+/* ---------------------------------------------------------------- options */
+
+#define OPW_SYNC_OVERLAP 0   /* per-tile flags: consumers start as tiles land */
+#define OPW_SYNC_SERIAL  1   /* consumers wait until EVERY tile is published
+                                (the "test with barrier sync first" debug mode
+                                of "Triton-distributed Semantics", Best Practices 8) */
+
+#define OPW_SCHED_SWIZZLE 0  /* static: CTA c starts on home rank c mod R and
+                                rotates ("Threadblock Swizzling") */
+#define OPW_SCHED_READY   1  /* dynamic: CTAs claim output tiles from a device
+                                counter in the order their rows are published */
+
+#define OPW_ROLE_FUSED    0  /* producer warps and consumer warps together */
+#define OPW_ROLE_PRODUCER 1  /* only the gather + publish (for overlap timing) */
+#define OPW_ROLE_CONSUMER 2  /* only wait + GEMM; the epoch must already be
+                                published by an earlier producer launch */
+
+#define OPW_FAULT_NONE        0
+#define OPW_FAULT_DROP_TILE   1  /* the producer never publishes flag slot fault_arg */
+#define OPW_FAULT_STALE_EPOCH 2  /* the producer publishes epoch-1 into slot fault_arg */
+
+typedef struct {
+    uint64_t timeout_ns;          /* bound on every device-side wait; 0 = 2e9 (2 s) */
+    int32_t sync_mode;            /* OPW_SYNC_* */
+    int32_t schedule;             /* OPW_SCHED_* */
+    int32_t role;                 /* OPW_ROLE_* */
+    int32_t num_ctas;             /* persistent grid size; 0 = one CTA per SM */
+    const int32_t* publish_perm;  /* host [R] or NULL: rank publish_perm[i] is published
+                                     i-th, and none of its tiles before every tile of
+                                     rank publish_perm[i-1] is published.  NULL: ranks
+                                     interleaved row block by row block. */
+    const uint32_t* delay_ns;     /* host [R] or NULL: no copy of rank r starts earlier
+                                     than delay_ns[r] after its CTA started */
+    uint64_t* trace_dev;          /* device [opw_ag_trace_words()] or NULL; see below */
+    int32_t fault_kind;           /* OPW_FAULT_* (fault injection on the host-chosen slot) */
+    int32_t fault_arg;
+} opw_opts;
+
+/* Fill *o with the defaults (all fields 0 / NULL). */
+void opw_opts_default(opw_opts* o);
+
+/* ---------------------------------------------------------------- AG-GEMM */
+
+/*
+ * Flag tile (square, in elements) used for shapes (M_r, K): 128 when both
+ * are multiples of 128, else 64.  Flag slot of tile (r, mt, kt):
+ * (r * (M_r/ft) + mt) * (K/ft) + kt.  Returns the slot count, or -1 for
+ * invalid sizes.
+ */
+int64_t opw_ag_flag_tile(int64_t M_r, int64_t K);
+int64_t opw_ag_num_flags(int32_t R, int64_t M_r, int64_t K);
+
+/*
+ * Trace layout (uint64 words), written only when opts.trace_dev != NULL:
+ *   [0, F)            publish time (%globaltimer ns) of each flag slot
+ *   [F, 2F)           earliest time a consumer's acquire of the slot
+ *                     succeeded (atomicMin; the caller fills this range
+ *                     with all-ones bits before the launch)
+ *   [2F, 2F+T)        per output tile: (cta << 32) | visit position
+ *   [2F+T, 2F+2T)     per output tile: time its first A load was issued
+ *   [2F+2T, 2F+2T+G)  per CTA: start time
+ * with F = opw_ag_num_flags(), T = ceil(M/128)*ceil(N/256), G = grid size
+ * (at most OPW_TRACE_MAX_CTAS words are reserved).
+ */
+#define OPW_TRACE_MAX_CTAS 1024
+int64_t opw_ag_trace_words(int32_t R, int64_t M_r, int64_t N, int64_t K);
+
+/*
+ * AllGather -> GEMM ("AllGather and GEMM Overlapping"):
+ *   G = concat(A_0, ..., A_{R-1})  along rows        (the AllGather)
+ *   C = G * B                       fp32 accumulate, bf16 round-to-nearest-even
+ *
+ *   symm    : logical heap; A_r = [M_r, K] bf16 at heap_dev + rank_off[r] + a_off.
+ *   B_dev   : [K, N] bf16.
+ *   G_dev   : [R*M_r, K] bf16 gathered buffer, written by the producer warps.
+ *   C_dev   : [R*M_r, N] bf16 output.
+ *   sig     : at least opw_ag_num_flags(R, M_r, K) slots.
+ *   epoch   : opw_signal_next_epoch() for FUSED / PRODUCER roles; for the
+ *             CONSUMER role, the epoch an earlier PRODUCER launch published.
+ *   opts    : NULL = defaults.
+ *
+ * Producer warps copy each flag tile of each A_r into G with TMA, wait for the
+ * copy to complete, then publish flags[slot] = epoch with a .gpu release.
+ * Consumer warps acquire each flag (>= epoch) before their TMA loads read that
+ * tile of G, then run tcgen05 MMAs with TMEM accumulators.  After the launch
+ * every flag slot holds `epoch` and G is bit-identical to the concatenation.
+ *
+ * Shapes: M_r, K multiples of 64 (flag tile 64) or 128; N a multiple of 8;
+ * R*M_r, N, K <= 2^31.  Alignment: heap_dev, B_dev, G_dev, C_dev, a_off and
+ * rank_off[] multiples of 16 bytes.  G and C must not overlap any A_r or B.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, BAD_EPOCH, NOT_READY,
+ * CUDA (launch failure).  Device errors (TIMEOUT, FLAG_PROTOCOL) surface at
+ * opw_status_sync().
+ */
+opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t N, int64_t K,
+                       const void* B_dev, void* G_dev, void* C_dev, opw_signal* sig,
+                       uint64_t epoch, const opw_opts* opts, void* stream);
+
+/* ---------------------------------------------------------------- GEMM-RS */
+
+/* Flag slots for GEMM-RS outputs: 128x128 tiles of each rank's [M/R, N]
+ * block, slot (j * (M/R/128) + mt) * ceil(N/128) + nt.  -1 if invalid. */
+int64_t opw_rs_num_flags(int32_t R, int64_t M, int64_t N);
+
+/*
+ * GEMM -> ReduceScatter ("GEMM and ReduceScatter Overlapping"):
+ *   P_r   = A_r * B_r                  (fresh fp32 TMEM accumulator per rank)
+ *   S     = (((0 + P_0) + P_1) + ...)  fp32 adds in rank order 0..R-1
+ *   out_j = bf16_rne(rows [j*M/R, (j+1)*M/R) of S), stored in rank j's slice
+ *
+ *   A_r   = [M, K_r] bf16 at heap_dev + rank_off[r] + a_off
+ *   B_r   = [K_r, N] bf16 at heap_dev + rank_off[r] + b_off
+ *   out_j = [M/R, N] bf16 at heap_dev + rank_off[j] + out_off
+ *
+ * The MMA warp produces partial tiles into a double-buffered TMEM accumulator
+ * and signals each on an on-chip barrier; the reduction warps add them in
+ * rank order as they land, write each finished row block to its rank, and
+ * publish flags[slot] = epoch (.gpu release) per 128x128 output tile.
+ *
+ * Shapes: M a multiple of 128*R; K_r a multiple of 64; N a multiple of 8.
+ * Alignment and errors as for opw_ag_gemm.  `opts` fields used: timeout_ns,
+ * num_ctas (others must be defaults).
+ */
+opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t out_off,
+                       int64_t M, int64_t N, int64_t K_r, opw_signal* sig, uint64_t epoch,
+                       const opw_opts* opts, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OPW_H */

@@ -1,0 +1,628 @@
+// AllGather -> GEMM, tile by tile, in one persistent warp-specialised kernel.
+//
+// Follows "Triton-distributed Semantics": the producer copies every tile of
+// every rank's shard into the gathered buffer and signals it ("Producer-
+// Consumer Model", "AllGather and GEMM Overlapping" steps 1-2); the consumer
+// waits on each tile's signal, establishes the data dependency ("Token-Based
+// Data Dependency") and computes at once (step 3); consumers start on their
+// own rank's rows and rotate ("Threadblock Swizzling").
+//
+// One CTA per SM, 8 warps:
+//   warp 0     loader: acquires the flags of the A tiles a k-block needs, then
+//              TMA-loads the A tile from the gathered buffer G and the B tile
+//              into a 4-stage shared-memory ring.  Owns the tile schedule.
+//   warp 1     MMA: one thread issues tcgen05.mma (bf16 x bf16 -> fp32) into a
+//              double-buffered TMEM accumulator (2 x 128 lanes x 256 columns).
+//   warp 2     gather producer: TMA-copies flag tiles of A_r into G through
+//              shared memory, waits for the copy to complete, and publishes the
+//              tile's flag with st.release.gpu.
+//   warp 3     allocates / frees TMEM.
+//   warps 4-7  epilogue: tcgen05.ld -> bf16 (round to nearest even) ->
+//              swizzled shared memory -> TMA store of C.
+// Every wait is bounded: on timeout the kernel latches an error in the
+// signal object's status word, drains its own in-flight copies and MMAs,
+// frees TMEM and returns.
+#include "opw_device.cuh"
+#include "opw_kernels.h"
+
+namespace opw {
+namespace {
+
+struct AgCtrl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t gfull[2];
+    uint64_t tq_full[TILE_Q];
+    uint64_t tq_empty[TILE_Q];
+    uint64_t mma_done;
+    int32_t tile_q[TILE_Q];
+    uint32_t tmem_base;
+    int32_t abort;
+};
+
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
+constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE_BYTES;
+constexpr int OFF_GATHER = OFF_EPI + 4 * EPI_WARP_BYTES;
+constexpr int OFF_CTRL = OFF_GATHER + 2 * GATHER_BUF_BYTES;
+constexpr int SMEM_ALLOC = OFF_CTRL + static_cast<int>(sizeof(AgCtrl)) + 1024;
+static_assert(SMEM_ALLOC <= 232448, "shared memory budget (227 KiB per CTA)");
+static_assert(OFF_B % 1024 == 0 && OFF_EPI % 1024 == 0 && OFF_GATHER % 1024 == 0,
+              "swizzled buffers must be 1024-byte aligned");
+
+constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators of 256 columns
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, /*B MN-major*/ true);
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p)
+{
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Wait without giving up on an abort: used only to let this CTA's own
+// in-flight copies or MMAs land before it exits.  Still time-bounded.
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, const ErrCtx& e)
+{
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > e.timeout_ns) {
+            raise_error(e, OPW_ERR_TIMEOUT, -1, SITE_DRAIN);
+            return;
+        }
+    }
+}
+
+// Tile visited at position `idx` of the dynamic schedule: output rows in the
+// order their flag tiles are published, all column tiles of a row together.
+__device__ __forceinline__ int ready_tile(const AgParams& p, int idx)
+{
+    const int mp = idx / p.T_N;
+    const int n = idx - mp * p.T_N;
+    int m = mp;
+    if (p.ft == BM && p.M_r % BM == 0) {
+        const int tpr = p.M_r / BM;
+        if (p.has_perm) {
+            m = p.perm[mp / tpr] * tpr + mp % tpr;
+        } else {
+            m = (mp % p.R) * tpr + mp / p.R;
+        }
+    }
+    return m * p.T_N + n;
+}
+
+// Wait (whole warp) until every rank's publish counter shows all of its
+// tiles published for this epoch: the serial mode's grid-wide barrier.
+__device__ bool wait_all_published(const AgParams& p, const ErrCtx& ec)
+{
+    const uint32_t lane = lane_id();
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+        bool ok = true;
+        if (lane < static_cast<uint32_t>(p.R))
+            ok = ld_acquire_u64(p.counters + CTR_RANK_DONE + lane) >= p.rank_target[lane];
+        if (__all_sync(0xffffffffu, ok)) break;
+        __nanosleep(256);
+        if ((it & 7u) == 7u) {
+            if (aborted(ec)) return false;
+            if (globaltimer() - t0 > ec.timeout_ns) {
+                if (lane == 0) raise_error(ec, OPW_ERR_TIMEOUT, -1, SITE_SERIAL);
+                return false;
+            }
+        }
+    }
+    __syncwarp();
+    if (lane == 0) fence_acq_rel_gpu();
+    __syncwarp();
+    return true;
+}
+
+// One polling round over the flags of k-columns [ready_kt, ready_kt + 32):
+// lane i acquires column ready_kt + i in each flag row the tile covers.
+// Returns how many leading columns are published (>= epoch).
+__device__ __forceinline__ int poll_flags(const AgParams& p, int base0, int base1, int ready_kt)
+{
+    const uint32_t lane = lane_id();
+    const int kt = ready_kt + static_cast<int>(lane);
+    bool ready = true;
+    if (kt < p.T_k) {
+        const int64_t e = static_cast<int64_t>(p.epoch);
+        ready = ld_acquire(p.flags + base0 + kt) >= e;
+        if (base1 >= 0) ready = ready && (ld_acquire(p.flags + base1 + kt) >= e);
+    }
+    const uint32_t mask = __ballot_sync(0xffffffffu, ready);
+    int n = (mask == 0xffffffffu) ? 32 : (__ffs(~mask) - 1);
+    if (ready_kt + n > p.T_k) n = p.T_k - ready_kt;
+    if (n > 0 && p.trace != nullptr && static_cast<int>(lane) < n) {
+        const uint64_t now = globaltimer();
+        const int F = p.R * p.T_mr * p.T_k;
+        atomicMin(reinterpret_cast<unsigned long long*>(p.trace + F + base0 + kt), now);
+        if (base1 >= 0)
+            atomicMin(reinterpret_cast<unsigned long long*>(p.trace + F + base1 + kt), now);
+    }
+    return n;
+}
+
+// ------------------------------------------------------------------ loader
+
+__device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const ErrCtx& ec)
+{
+    const uint32_t lane = lane_id();
+    const int G = static_cast<int>(gridDim.x);
+    const int c = static_cast<int>(blockIdx.x);
+    const int T = p.T_M * p.T_N;
+    const int KB = p.K / BK;
+
+    // Static schedule: this CTA owns tiles q = c + i*G; it starts at the first
+    // one in its home rank's rows (h*tiles_per_pe row tiles down) and wraps.
+    const int n_mine = c < T ? (T - c + G - 1) / G : 0;
+    const int h = c % p.R;
+    const long long start_q = static_cast<long long>(h) * (p.T_M / p.R) * p.T_N;
+    int i0 = start_q <= c ? 0 : static_cast<int>((start_q - c + G - 1) / G);
+    if (i0 >= n_mine) i0 = 0;
+
+    uint32_t stage = 0, sphase = 0, tq = 0, tqphase = 0;
+    uint32_t filled = 0, last_par = 0;
+    bool ok = true;
+    bool serial_pending = (p.sync_mode == OPW_SYNC_SERIAL);
+
+    for (int s = 0; ok; ++s) {
+        int q;
+        if (p.schedule == OPW_SCHED_READY) {
+            long long idx = 0;
+            if (lane == 0)
+                idx = static_cast<long long>(atomicAdd(p.counters + CTR_CLAIM, 1ull) - p.claim_base);
+            idx = __shfl_sync(0xffffffffu, idx, 0);
+            q = idx < T ? ready_tile(p, static_cast<int>(idx)) : -1;
+        } else {
+            q = s < n_mine ? c + ((i0 + s) % n_mine) * G : -1;
+        }
+
+        // Hand the tile to the MMA and epilogue warps (-1 = no more work).
+        if (!wait_bar(&ctrl->tq_empty[tq], tqphase ^ 1u, ec, SITE_TILE_QUEUE)) break;
+        if (lane == 0) {
+            reinterpret_cast<volatile int32_t*>(ctrl->tile_q)[tq] = q;
+            mbar_arrive(&ctrl->tq_full[tq]);
+        }
+        __syncwarp();
+        if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
+        if (q < 0) break;
+
+        const int m0 = (q / p.T_N) * BM;
+        const int n0 = (q % p.T_N) * BN;
+        if (p.trace != nullptr && lane == 0) {
+            const int F = p.R * p.T_mr * p.T_k;
+            p.trace[2 * F + q] = (static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(s);
+        }
+        if (serial_pending) {
+            if (!wait_all_published(p, ec)) break;
+            serial_pending = false;
+        }
+
+        // Flag rows covered by rows [m0, m0 + BM): one (flag tile 128) or two (64).
+        int base0, base1 = -1;
+        {
+            const int r = m0 / p.M_r;
+            const int mt = (m0 - r * p.M_r) / p.ft;
+            base0 = (r * p.T_mr + mt) * p.T_k;
+            if (p.ft < BM && m0 + p.ft < p.M) {
+                const int g = m0 + p.ft;
+                const int r1 = g / p.M_r;
+                const int mt1 = (g - r1 * p.M_r) / p.ft;
+                base1 = (r1 * p.T_mr + mt1) * p.T_k;
+            }
+        }
+
+        int ready_kt = 0;
+        bool fresh = false;  // flags acquired since the last TMA issue
+        uint64_t wait_t0 = 0;
+        for (int kb = 0; kb < KB && ok; ++kb) {
+            const int kt = (kb * BK) / p.ft;
+            // Acquire: no load of this A tile before its flag shows the epoch.
+            uint32_t spins = 0;
+            while (kt >= ready_kt) {
+                const int n = poll_flags(p, base0, base1, ready_kt);
+                if (n > 0) {
+                    ready_kt += n;
+                    fresh = true;
+                    spins = 0;
+                    continue;
+                }
+                if (spins == 0) wait_t0 = globaltimer();
+                ++spins;
+                __nanosleep(128);
+                if ((spins & 7u) == 0) {
+                    if (aborted(ec)) { ok = false; break; }
+                    if (globaltimer() - wait_t0 > ec.timeout_ns) {
+                        if (lane == 0) {
+                            // report the first missing slot
+                            const int slot = base0 + ready_kt;
+                            const int rank = slot / (p.T_mr * p.T_k);
+                            raise_error(ec, OPW_ERR_TIMEOUT, rank, slot);
+                        }
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (!ok) break;
+            __syncwarp();
+            if (!wait_bar(&ctrl->empty[stage], sphase ^ 1u, ec, SITE_LOADER_EMPTY)) { ok = false; break; }
+            if (lane == 0) {
+                // consume_token: order the flag acquires (made by every lane of
+                // this warp) before the async-proxy reads of the tile.
+                if (fresh) {
+                    fence_acq_rel_gpu();
+                    fence_async_global();
+                }
+                if (kb == 0 && p.trace != nullptr) {
+                    const int F = p.R * p.T_mr * p.T_k;
+                    p.trace[2 * F + T + q] = globaltimer();
+                }
+                uint64_t* fb = &ctrl->full[stage];
+                mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
+                tma_load_2d(smem + OFF_A + stage * A_STAGE_BYTES, &p.g_load, fb, kb * BK, m0);
+                uint8_t* bs = smem + OFF_B + stage * B_STAGE_BYTES;
+#pragma unroll
+                for (int j = 0; j < BN / 64; ++j)
+                    tma_load_2d(bs + j * B_CHUNK_BYTES, &p.b_load, fb, n0 + 64 * j, kb * BK);
+            }
+            __syncwarp();
+            fresh = false;
+            filled |= 1u << stage;
+            last_par = (last_par & ~(1u << stage)) | (sphase << stage);
+            if (++stage == STAGES) { stage = 0; sphase ^= 1u; }
+        }
+    }
+    // Every TMA load this warp issued must land before the CTA may exit.
+    for (int st = 0; st < STAGES; ++st)
+        if (filled & (1u << st)) drain_bar(&ctrl->full[st], (last_par >> st) & 1u, ec);
+}
+
+// ------------------------------------------------------------------ MMA
+
+__device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t tmem,
+                        const ErrCtx& ec)
+{
+    const uint32_t lane = lane_id();
+    const int KB = p.K / BK;
+    const uint32_t a_base = smem_u32(smem + OFF_A);
+    const uint32_t b_base = smem_u32(smem + OFF_B);
+    uint32_t stage = 0, sphase = 0, acc = 0, aphase = 0, tq = 0, tqphase = 0;
+    bool ok = true;
+    while (ok) {
+        if (!wait_bar(&ctrl->tq_full[tq], tqphase, ec, SITE_TILE_QUEUE)) break;
+        const int q = reinterpret_cast<volatile int32_t*>(ctrl->tile_q)[tq];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctrl->tq_empty[tq]);
+        if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
+        if (q < 0) break;
+
+        if (!wait_bar(&ctrl->tmem_empty[acc], aphase ^ 1u, ec, SITE_MMA_TMEM_EMPTY)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+            if (!wait_bar(&ctrl->full[stage], sphase, ec, SITE_MMA_FULL)) { ok = false; break; }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t as = a_base + stage * A_STAGE_BYTES;
+                const uint32_t bs = b_base + stage * B_STAGE_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / UMMA_K; ++k) {
+                    // A: K-major, rows 128 B apart, 8-row groups 1024 B apart;
+                    //    k steps of 16 elements advance 32 B inside the swizzled row.
+                    const uint64_t ad = sdesc_sw128(as + k * (UMMA_K * 2), 16, 1024);
+                    // B: N-major, 64-column chunks 8 KiB apart (LBO), 8-row K groups
+                    //    1024 B apart (SBO); k steps of 16 rows advance 2 KiB.
+                    const uint64_t bd = sdesc_sw128(bs + k * (UMMA_K * 128), B_CHUNK_BYTES, 1024);
+                    mma_bf16(d, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                }
+                mma_commit(&ctrl->empty[stage]);  // frees the stage when these MMAs finish
+            }
+            __syncwarp();
+            if (++stage == STAGES) { stage = 0; sphase ^= 1u; }
+        }
+        if (!ok) break;
+        if (lane == 0) mma_commit(&ctrl->tmem_full[acc]);
+        __syncwarp();
+        if (++acc == 2) { acc = 0; aphase ^= 1u; }
+    }
+    // Every MMA issued must complete before TMEM is released.
+    if (lane == 0) mma_commit(&ctrl->mma_done);
+    __syncwarp();
+    drain_bar(&ctrl->mma_done, 0, ec);
+}
+
+// ------------------------------------------------------------------ epilogue
+
+__device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t tmem,
+                             const ErrCtx& ec, int warp)
+{
+    const uint32_t lane = lane_id();
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
+    uint8_t* buf = smem + OFF_EPI + quarter * EPI_WARP_BYTES;
+    const uint32_t row_addr = smem_u32(buf) + lane * 128u;
+    uint32_t acc = 0, aphase = 0, tq = 0, tqphase = 0;
+    while (true) {
+        if (!wait_bar(&ctrl->tq_full[tq], tqphase, ec, SITE_TILE_QUEUE)) break;
+        const int q = reinterpret_cast<volatile int32_t*>(ctrl->tile_q)[tq];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctrl->tq_empty[tq]);
+        if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
+        if (q < 0) break;
+
+        const int m0 = (q / p.T_N) * BM;
+        const int n0 = (q % p.T_N) * BN;
+        const int row0 = m0 + quarter * 32;
+        if (!wait_bar(&ctrl->tmem_full[acc], aphase, ec, SITE_EPI_TMEM_FULL)) break;
+        tc_fence_after();
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 64; ++ch) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(taddr + ch * 64, v0);
+            tmem_ld32(taddr + ch * 64 + 32, v1);
+            tmem_ld_wait(v0);
+            tmem_ld_wait(v1);
+            if (ch == BN / 64 - 1) {
+                // accumulator fully read: the MMA warp may reuse it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctrl->tmem_empty[acc]);
+            }
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                w[i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
+                w[16 + i] = pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
+            }
+            // the previous TMA store must have finished reading the staging rows
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+            // row `lane`, 16-byte chunk j stored at chunk j ^ (row & 7): the
+            // 128-byte swizzle the C tensor map expects
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), w[4 * j],
+                             w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0 && row0 < p.M && n0 + ch * 64 < p.N) {
+                tma_store_2d(&p.c_store, buf, n0 + ch * 64, row0);
+                bulk_commit();
+            }
+            __syncwarp();
+        }
+        if (++acc == 2) { acc = 0; aphase ^= 1u; }
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+}
+
+// ------------------------------------------------------------------ gather producer
+
+__device__ void run_gather(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const ErrCtx& ec,
+                           uint64_t t_start)
+{
+    const uint32_t lane = lane_id();
+    const int G = static_cast<int>(gridDim.x);
+    const int c = static_cast<int>(blockIdx.x);
+    const int per_rank = p.T_mr * p.T_k;
+    const int n_items = p.R * per_rank;
+    const int subs = p.ft / GATHER_SUB_ROWS;
+    const uint32_t sub_bytes = static_cast<uint32_t>(p.ft) * GATHER_SUB_ROWS * 2u;
+    const int n_mine = c < n_items ? (n_items - c + G - 1) / G : 0;
+    uint8_t* buf0 = smem + OFF_GATHER;
+    int ordered_upto = 0;  // rank positions whose predecessors are known complete
+    uint32_t seq = 0;      // sub-box sequence number: buffer seq & 1, phase (seq >> 1) & 1
+    bool ok = true;
+
+    for (int it = 0; it < n_mine && ok; ++it) {
+        const int pidx = c + it * G;
+        int r, mt, kt, ip = 0;
+        if (p.has_perm) {
+            // rank-major in publish order
+            ip = pidx / per_rank;
+            r = p.perm[ip];
+            const int rem = pidx - ip * per_rank;
+            mt = rem / p.T_k;
+            kt = rem - mt * p.T_k;
+        } else {
+            // row block by row block, ranks interleaved, k fastest
+            mt = pidx / (p.R * p.T_k);
+            const int rem = pidx - mt * p.R * p.T_k;
+            r = rem / p.T_k;
+            kt = rem - r * p.T_k;
+        }
+
+        // Skewed readiness: rank r starts no earlier than delay_ns[r] ...
+        if (p.has_delay) {
+            const uint64_t d = p.delay_ns[r] < ec.timeout_ns ? p.delay_ns[r] : ec.timeout_ns;
+            while (globaltimer() - t_start < d) __nanosleep(256);
+        }
+        // ... and only after every tile of the rank published before it.
+        if (p.has_perm && ip > 0 && ordered_upto < ip) {
+            const uint64_t target = p.rank_target[p.perm[ip - 1]];
+            const unsigned long long* ctr = p.counters + CTR_RANK_DONE + p.perm[ip - 1];
+            const uint64_t t0 = globaltimer();
+            for (uint32_t s = 0;; ++s) {
+                uint32_t done = 0;
+                if (lane == 0) done = ld_acquire_u64(ctr) >= target ? 1u : 0u;
+                done = __shfl_sync(0xffffffffu, done, 0);
+                if (done) break;
+                __nanosleep(256);
+                if ((s & 7u) == 7u) {
+                    if (aborted(ec)) { ok = false; break; }
+                    if (globaltimer() - t0 > ec.timeout_ns) {
+                        if (lane == 0) raise_error(ec, OPW_ERR_TIMEOUT, p.perm[ip - 1], SITE_SKEW_ORDER);
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (!ok) break;
+            ordered_upto = ip;
+        }
+
+        // Copy the flag tile 32 rows at a time through two staging buffers:
+        // TMA load A_r rows -> shared, then TMA store shared -> G.
+        const int x = kt * p.ft;
+        const int y_src = mt * p.ft;
+        const int y_dst = r * p.M_r + mt * p.ft;
+        auto issue_load = [&](uint32_t sq, int sub) {
+            if (lane == 0) {
+                bulk_wait_read<0>();  // earlier stores are done reading the staging buffer
+                uint64_t* fb = &ctrl->gfull[sq & 1u];
+                mbar_arrive_expect_tx(fb, sub_bytes);
+                tma_load_2d(buf0 + (sq & 1u) * GATHER_BUF_BYTES, &p.shard[r], fb, x,
+                            y_src + sub * GATHER_SUB_ROWS);
+            }
+            __syncwarp();
+        };
+        issue_load(seq, 0);
+        for (int sub = 0; sub < subs; ++sub) {
+            if (sub + 1 < subs) issue_load(seq + 1, sub + 1);
+            if (!wait_bar(&ctrl->gfull[seq & 1u], (seq >> 1) & 1u, ec, SITE_GATHER_LOAD)) {
+                // both outstanding loads must land before the CTA may exit
+                drain_bar(&ctrl->gfull[seq & 1u], (seq >> 1) & 1u, ec);
+                if (sub + 1 < subs) drain_bar(&ctrl->gfull[(seq + 1) & 1u], ((seq + 1) >> 1) & 1u, ec);
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                tma_store_2d(&p.g_store, buf0 + (seq & 1u) * GATHER_BUF_BYTES, x,
+                             y_dst + sub * GATHER_SUB_ROWS);
+                bulk_commit();
+            }
+            __syncwarp();
+            ++seq;
+        }
+        if (!ok) break;
+
+        // Publish: the copy is complete, then release the flag (SET epoch).
+        if (lane == 0) {
+            bulk_wait<0>();
+            fence_async_global();
+            const int slot = (r * p.T_mr + mt) * p.T_k + kt;
+            int64_t v = static_cast<int64_t>(p.epoch);
+            bool skip = false;
+            if (p.fault_kind == OPW_FAULT_DROP_TILE && slot == p.fault_arg) skip = true;
+            if (p.fault_kind == OPW_FAULT_STALE_EPOCH && slot == p.fault_arg) v -= 1;
+            // the publish time is read before the release, so no consumer can
+            // observe the flag earlier than the recorded time
+            const uint64_t t_pub = p.trace != nullptr ? globaltimer() : 0;
+            if (!skip) st_release(p.flags + slot, v);
+            red_release_add(p.counters + CTR_RANK_DONE + r, 1ull);
+            if (p.trace != nullptr) p.trace[slot] = t_pub;
+        }
+        __syncwarp();
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+}
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__ AgParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    AgCtrl* ctrl = reinterpret_cast<AgCtrl*>(smem + OFF_CTRL);
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
+    const bool consumer = p.role != OPW_ROLE_PRODUCER;
+    const bool producer = p.role != OPW_ROLE_CONSUMER;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&ctrl->full[i], 1);
+            mbar_init(&ctrl->empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctrl->tmem_full[i], 1);
+            mbar_init(&ctrl->tmem_empty[i], 4);
+            mbar_init(&ctrl->gfull[i], 1);
+        }
+        for (int i = 0; i < TILE_Q; ++i) {
+            mbar_init(&ctrl->tq_full[i], 1);
+            mbar_init(&ctrl->tq_empty[i], 1 + 4);
+        }
+        mbar_init(&ctrl->mma_done, 1);
+        // A device error latched by an earlier launch: do nothing.
+        ctrl->abort = ld_relaxed_s32(p.status) != 0 ? 1 : 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (ctrl->abort) return;
+
+    if (warp == 3 && consumer) {
+        tmem_alloc(&ctrl->tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 32) {
+        prefetch_tmap(&p.g_load);
+        prefetch_tmap(&p.b_load);
+        prefetch_tmap(&p.c_store);
+        prefetch_tmap(&p.g_store);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctrl->tmem_base;
+    const ErrCtx ec{p.status, &ctrl->abort, p.timeout_ns};
+    const uint64_t t_start = globaltimer();
+    if (p.trace != nullptr && threadIdx.x == 0) {
+        const int F = p.R * p.T_mr * p.T_k;
+        const int T = p.T_M * p.T_N;
+        if (blockIdx.x < OPW_TRACE_MAX_CTAS) p.trace[2 * F + 2 * T + blockIdx.x] = t_start;
+    }
+
+    if (warp == 0) {
+        if (consumer) run_loader(p, smem, ctrl, ec);
+    } else if (warp == 1) {
+        if (consumer) run_mma(p, smem, ctrl, tmem, ec);
+    } else if (warp == 2) {
+        if (producer) run_gather(p, smem, ctrl, ec, t_start);
+    } else if (warp >= 4) {
+        if (consumer) run_epilogue(p, smem, ctrl, tmem, ec, warp);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 3 && consumer) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+size_t ag_smem_bytes() { return SMEM_ALLOC; }
+
+cudaError_t launch_ag_gemm(const AgParams& p, int grid, cudaStream_t s)
+{
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        err = cudaFuncSetAttribute(ag_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   SMEM_ALLOC);
+        if (err != cudaSuccess) return err;
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ag_gemm_kernel, p);
+}
+
+}  // namespace opw

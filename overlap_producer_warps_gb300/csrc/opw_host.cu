@@ -1,0 +1,446 @@
+// Host side of the C ABI declared in include/opw.h: argument validation,
+// signal objects (flags, epochs, status word, counters), tensor-map
+// encoding and the cooperative launches.  Nothing here prints, throws or
+// allocates except opw_signal_alloc.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/opw.h"
+#include "opw_kernels.h"
+
+using namespace opw;
+
+// ---------------------------------------------------------------- signal object
+
+struct opw_signal {
+    int device;
+    int64_t num_slots;
+    void* mem;                     // one device allocation: flags | status | counters
+    int64_t* flags;                // [num_slots]
+    int32_t* status;               // [4]: code, rank, slot, reserved
+    unsigned long long* counters;  // [CTR_WORDS]
+    uint64_t epoch_last;           // last epoch published (host view)
+    uint64_t rank_done[OPW_MAX_RANKS];       // expected rank counters after all enqueued launches
+    uint64_t rank_target_last[OPW_MAX_RANKS];  // targets of the last producing launch
+    uint64_t claim_next;           // claim counter value after all enqueued launches
+    bool latched;                  // opw_status_sync saw a device error
+};
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+__global__ void signal_reset_kernel(int64_t* flags, int64_t n, int32_t* status,
+                                    unsigned long long* counters)
+{
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+        flags[i] = 0;
+    if (blockIdx.x == 0) {
+        if (threadIdx.x < 4) status[threadIdx.x] = 0;
+        if (threadIdx.x < CTR_WORDS) counters[threadIdx.x] = 0;
+    }
+}
+
+opw_status reset_device(opw_signal* s, cudaStream_t st)
+{
+    int blocks = static_cast<int>((s->num_slots + 255) / 256);
+    if (blocks < 1) blocks = 1;
+    if (blocks > 1024) blocks = 1024;
+    signal_reset_kernel<<<blocks, 256, 0, st>>>(s->flags, s->num_slots, s->status, s->counters);
+    if (cudaGetLastError() != cudaSuccess) return OPW_ERR_CUDA;
+    s->epoch_last = 0;
+    for (int r = 0; r < OPW_MAX_RANKS; ++r) s->rank_done[r] = s->rank_target_last[r] = 0;
+    s->claim_next = 0;
+    s->latched = false;
+    return OPW_OK;
+}
+
+// ---------------------------------------------------------------- CUDA helpers
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 row-major tensor [rows, cols] (row stride = cols elements).
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+              uint32_t box_rows, CUtensorMapSwizzle sw)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count(int dev)
+{
+    static int cache[64] = {};
+    if (dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned16(int64_t v) { return (v & 15) == 0; }
+
+const opw_opts& opts_or_default(const opw_opts* o, opw_opts& tmp)
+{
+    if (o != nullptr) return *o;
+    opw_opts_default(&tmp);
+    return tmp;
+}
+
+opw_status check_symm(const opw_symm* s)
+{
+    if (s == nullptr || s->heap_dev == nullptr || s->rank_off == nullptr) return OPW_ERR_INVALID_ARG;
+    if (s->R < 1 || s->R > OPW_MAX_RANKS || s->reserved != 0) return OPW_ERR_INVALID_ARG;
+    if (!aligned16(s->heap_dev)) return OPW_ERR_MISALIGNED;
+    for (int r = 0; r < s->R; ++r) {
+        if (s->rank_off[r] < 0) return OPW_ERR_INVALID_ARG;
+        if (!aligned16(s->rank_off[r])) return OPW_ERR_MISALIGNED;
+    }
+    return OPW_OK;
+}
+
+int grid_for(const opw_opts& o, int dev)
+{
+    const int sms = sm_count(dev);
+    if (sms <= 0) return 0;
+    if (o.num_ctas > 0 && o.num_ctas < sms) return o.num_ctas;
+    return sms;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- C ABI
+
+extern "C" {
+
+const char* opw_status_str(opw_status s)
+{
+    switch (s) {
+    case OPW_OK: return "OK";
+    case OPW_ERR_INVALID_ARG: return "INVALID_ARG";
+    case OPW_ERR_UNSUPPORTED_SHAPE: return "UNSUPPORTED_SHAPE";
+    case OPW_ERR_MISALIGNED: return "MISALIGNED";
+    case OPW_ERR_BAD_EPOCH: return "BAD_EPOCH";
+    case OPW_ERR_CUDA: return "CUDA_ERROR";
+    case OPW_ERR_TIMEOUT: return "TIMEOUT";
+    case OPW_ERR_FLAG_PROTOCOL: return "FLAG_PROTOCOL";
+    case OPW_ERR_NOT_READY: return "NOT_READY";
+    default: return "UNKNOWN";
+    }
+}
+
+int32_t opw_abi_version(void) { return OPW_ABI_VERSION; }
+
+void opw_opts_default(opw_opts* o)
+{
+    if (o != nullptr) std::memset(o, 0, sizeof(*o));
+}
+
+opw_status opw_signal_alloc(opw_signal** out, int64_t num_slots, void* stream)
+{
+    if (out == nullptr) return OPW_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (num_slots < 1 || num_slots > (int64_t(1) << 40)) return OPW_ERR_INVALID_ARG;
+    opw_signal* s = new (std::nothrow) opw_signal();
+    if (s == nullptr) return OPW_ERR_CUDA;
+    if (cudaGetDevice(&s->device) != cudaSuccess) {
+        delete s;
+        return OPW_ERR_CUDA;
+    }
+    const size_t flag_bytes = static_cast<size_t>(num_slots) * sizeof(int64_t);
+    const size_t status_off = (flag_bytes + 255) & ~size_t(255);
+    const size_t ctr_off = status_off + 256;
+    const size_t total = ctr_off + CTR_WORDS * sizeof(unsigned long long);
+    if (cudaMalloc(&s->mem, total) != cudaSuccess) {
+        delete s;
+        return OPW_ERR_CUDA;
+    }
+    s->num_slots = num_slots;
+    s->flags = static_cast<int64_t*>(s->mem);
+    s->status = reinterpret_cast<int32_t*>(static_cast<char*>(s->mem) + status_off);
+    s->counters = reinterpret_cast<unsigned long long*>(static_cast<char*>(s->mem) + ctr_off);
+    if (reset_device(s, static_cast<cudaStream_t>(stream)) != OPW_OK) {
+        cudaFree(s->mem);
+        delete s;
+        return OPW_ERR_CUDA;
+    }
+    *out = s;
+    return OPW_OK;
+}
+
+opw_status opw_signal_reset(opw_signal* sig, void* stream)
+{
+    if (sig == nullptr) return OPW_ERR_INVALID_ARG;
+    return reset_device(sig, static_cast<cudaStream_t>(stream));
+}
+
+opw_status opw_signal_free(opw_signal* sig)
+{
+    if (sig == nullptr) return OPW_OK;
+    const cudaError_t e = cudaFree(sig->mem);
+    delete sig;
+    return e == cudaSuccess ? OPW_OK : OPW_ERR_CUDA;
+}
+
+opw_status opw_signal_next_epoch(const opw_signal* sig, uint64_t* epoch)
+{
+    if (sig == nullptr || epoch == nullptr) return OPW_ERR_INVALID_ARG;
+    *epoch = sig->epoch_last + 1;
+    return OPW_OK;
+}
+
+opw_status opw_signal_flags(const opw_signal* sig, int64_t** flags_dev, int64_t* num_slots)
+{
+    if (sig == nullptr) return OPW_ERR_INVALID_ARG;
+    if (flags_dev != nullptr) *flags_dev = sig->flags;
+    if (num_slots != nullptr) *num_slots = sig->num_slots;
+    return OPW_OK;
+}
+
+opw_status opw_status_sync(opw_signal* sig, void* stream, int32_t* rank, int32_t* tile)
+{
+    if (sig == nullptr) return OPW_ERR_INVALID_ARG;
+    if (rank != nullptr) *rank = -1;
+    if (tile != nullptr) *tile = -1;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return OPW_ERR_CUDA;
+    int32_t h[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(h, sig->status, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return OPW_ERR_CUDA;
+    if (h[0] != OPW_OK) {
+        sig->latched = true;
+        if (rank != nullptr) *rank = h[1];
+        if (tile != nullptr) *tile = h[2];
+    }
+    return h[0];
+}
+
+int64_t opw_ag_flag_tile(int64_t M_r, int64_t K)
+{
+    if (M_r <= 0 || K <= 0) return -1;
+    if (M_r % 128 == 0 && K % 128 == 0) return 128;
+    if (M_r % 64 == 0 && K % 64 == 0) return 64;
+    return -1;
+}
+
+int64_t opw_ag_num_flags(int32_t R, int64_t M_r, int64_t K)
+{
+    const int64_t ft = opw_ag_flag_tile(M_r, K);
+    if (ft < 0 || R < 1 || R > OPW_MAX_RANKS) return -1;
+    return static_cast<int64_t>(R) * (M_r / ft) * (K / ft);
+}
+
+int64_t opw_ag_trace_words(int32_t R, int64_t M_r, int64_t N, int64_t K)
+{
+    const int64_t F = opw_ag_num_flags(R, M_r, K);
+    if (F < 0 || N <= 0) return -1;
+    const int64_t T = ((R * M_r + BM - 1) / BM) * ((N + BN - 1) / BN);
+    return 2 * F + 2 * T + OPW_TRACE_MAX_CTAS;
+}
+
+opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t N, int64_t K,
+                       const void* B_dev, void* G_dev, void* C_dev, opw_signal* sig,
+                       uint64_t epoch, const opw_opts* opts_in, void* stream)
+{
+    // ---- arguments (no CUDA call before every check has passed)
+    opw_status st = check_symm(symm);
+    if (st != OPW_OK) return st;
+    if (B_dev == nullptr || G_dev == nullptr || C_dev == nullptr || sig == nullptr)
+        return OPW_ERR_INVALID_ARG;
+    opw_opts tmp;
+    const opw_opts& o = opts_or_default(opts_in, tmp);
+    if (o.sync_mode != OPW_SYNC_OVERLAP && o.sync_mode != OPW_SYNC_SERIAL) return OPW_ERR_INVALID_ARG;
+    if (o.schedule != OPW_SCHED_SWIZZLE && o.schedule != OPW_SCHED_READY) return OPW_ERR_INVALID_ARG;
+    if (o.role < OPW_ROLE_FUSED || o.role > OPW_ROLE_CONSUMER) return OPW_ERR_INVALID_ARG;
+    if (o.fault_kind < OPW_FAULT_NONE || o.fault_kind > OPW_FAULT_STALE_EPOCH) return OPW_ERR_INVALID_ARG;
+    if (o.num_ctas < 0) return OPW_ERR_INVALID_ARG;
+    const int R = symm->R;
+    if (o.publish_perm != nullptr) {
+        bool seen[OPW_MAX_RANKS] = {};
+        for (int i = 0; i < R; ++i) {
+            const int r = o.publish_perm[i];
+            if (r < 0 || r >= R || seen[r]) return OPW_ERR_INVALID_ARG;
+            seen[r] = true;
+        }
+    }
+    const int64_t ft = opw_ag_flag_tile(M_r, K);
+    if (ft < 0 || N <= 0 || N % 8 != 0) return OPW_ERR_UNSUPPORTED_SHAPE;
+    const int64_t M = static_cast<int64_t>(R) * M_r;
+    if (M > (int64_t(1) << 31) || N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+        return OPW_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(B_dev) || !aligned16(G_dev) || !aligned16(C_dev) ||
+        !aligned16(static_cast<int64_t>(a_off)) ||
+        (o.trace_dev != nullptr && (reinterpret_cast<uintptr_t>(o.trace_dev) & 7u) != 0))
+        return OPW_ERR_MISALIGNED;
+    const int64_t F = static_cast<int64_t>(R) * (M_r / ft) * (K / ft);
+    if (sig->num_slots < F) return OPW_ERR_INVALID_ARG;
+    if (sig->latched) return OPW_ERR_NOT_READY;
+    const bool produces = o.role != OPW_ROLE_CONSUMER;
+    if (produces ? epoch != sig->epoch_last + 1 : (epoch != sig->epoch_last || epoch == 0))
+        return OPW_ERR_BAD_EPOCH;
+
+    // ---- launch
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != sig->device) return OPW_ERR_CUDA;
+    const int grid = grid_for(o, dev);
+    if (grid <= 0) return OPW_ERR_CUDA;
+
+    AgParams p;
+    std::memset(&p, 0, sizeof p);
+    char* heap = static_cast<char*>(symm->heap_dev);
+    for (int r = 0; r < R; ++r) {
+        if (!make_map(&p.shard[r], heap + symm->rank_off[r] + a_off, K, M_r, static_cast<uint32_t>(ft),
+                      GATHER_SUB_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return OPW_ERR_CUDA;
+    }
+    if (!make_map(&p.g_store, G_dev, K, M, static_cast<uint32_t>(ft), GATHER_SUB_ROWS,
+                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&p.g_load, G_dev, K, M, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&p.b_load, B_dev, N, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&p.c_store, C_dev, N, M, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+        return OPW_ERR_CUDA;
+    p.flags = sig->flags;
+    p.status = sig->status;
+    p.counters = sig->counters;
+    p.trace = o.trace_dev;
+    p.epoch = epoch;
+    p.timeout_ns = o.timeout_ns != 0 ? o.timeout_ns : kDefaultTimeoutNs;
+    p.claim_base = sig->claim_next;
+    p.R = R;
+    p.M_r = static_cast<int32_t>(M_r);
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.ft = static_cast<int32_t>(ft);
+    p.T_mr = static_cast<int32_t>(M_r / ft);
+    p.T_k = static_cast<int32_t>(K / ft);
+    p.T_M = static_cast<int32_t>((M + BM - 1) / BM);
+    p.T_N = static_cast<int32_t>((N + BN - 1) / BN);
+    p.role = o.role;
+    p.sync_mode = o.sync_mode;
+    p.schedule = o.schedule;
+    p.has_perm = o.publish_perm != nullptr;
+    p.has_delay = o.delay_ns != nullptr;
+    p.fault_kind = o.fault_kind;
+    p.fault_arg = o.fault_arg;
+    for (int i = 0; i < R; ++i) {
+        p.perm[i] = o.publish_perm != nullptr ? o.publish_perm[i] : i;
+        p.delay_ns[i] = o.delay_ns != nullptr ? o.delay_ns[i] : 0u;
+    }
+    const uint64_t per_rank = static_cast<uint64_t>(p.T_mr) * p.T_k;
+    for (int r = 0; r < R; ++r)
+        p.rank_target[r] = produces ? sig->rank_done[r] + per_rank : sig->rank_target_last[r];
+
+    if (launch_ag_gemm(p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return OPW_ERR_CUDA;
+
+    // ---- host bookkeeping for the next launch on this object
+    if (produces) {
+        sig->epoch_last = epoch;
+        for (int r = 0; r < R; ++r) {
+            sig->rank_target_last[r] = p.rank_target[r];
+            sig->rank_done[r] = p.rank_target[r];
+        }
+    }
+    if (o.role != OPW_ROLE_PRODUCER && o.schedule == OPW_SCHED_READY)
+        sig->claim_next += static_cast<uint64_t>(p.T_M) * p.T_N + static_cast<uint64_t>(grid);
+    return OPW_OK;
+}
+
+int64_t opw_rs_num_flags(int32_t R, int64_t M, int64_t N)
+{
+    if (R < 1 || R > OPW_MAX_RANKS || M <= 0 || N <= 0 || M % (128 * R) != 0) return -1;
+    return static_cast<int64_t>(R) * (M / R / 128) * ((N + 127) / 128);
+}
+
+opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t out_off, int64_t M,
+                       int64_t N, int64_t K_r, opw_signal* sig, uint64_t epoch,
+                       const opw_opts* opts_in, void* stream)
+{
+    opw_status st = check_symm(symm);
+    if (st != OPW_OK) return st;
+    if (sig == nullptr) return OPW_ERR_INVALID_ARG;
+    opw_opts tmp;
+    const opw_opts& o = opts_or_default(opts_in, tmp);
+    if (o.sync_mode != 0 || o.schedule != 0 || o.role != 0 || o.publish_perm != nullptr ||
+        o.delay_ns != nullptr || o.fault_kind != 0 || o.num_ctas < 0)
+        return OPW_ERR_INVALID_ARG;
+    const int R = symm->R;
+    if (M <= 0 || N <= 0 || K_r <= 0 || M % (128 * R) != 0 || N % 8 != 0 || K_r % 8 != 0)
+        return OPW_ERR_UNSUPPORTED_SHAPE;
+    if (M > (int64_t(1) << 31) || N > (int64_t(1) << 31) || K_r > (int64_t(1) << 31))
+        return OPW_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(static_cast<int64_t>(a_off)) || !aligned16(static_cast<int64_t>(b_off)) ||
+        !aligned16(static_cast<int64_t>(out_off)) ||
+        (o.trace_dev != nullptr && (reinterpret_cast<uintptr_t>(o.trace_dev) & 7u) != 0))
+        return OPW_ERR_MISALIGNED;
+    const int64_t F = opw_rs_num_flags(R, M, N);
+    if (F < 0 || sig->num_slots < F) return OPW_ERR_INVALID_ARG;
+    if (sig->latched) return OPW_ERR_NOT_READY;
+    if (epoch != sig->epoch_last + 1) return OPW_ERR_BAD_EPOCH;
+
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != sig->device) return OPW_ERR_CUDA;
+    const int grid = grid_for(o, dev);
+    if (grid <= 0) return OPW_ERR_CUDA;
+
+    RsParams p;
+    std::memset(&p, 0, sizeof p);
+    const int64_t Mb = M / R;
+    char* heap = static_cast<char*>(symm->heap_dev);
+    for (int r = 0; r < R; ++r) {
+        char* base = heap + symm->rank_off[r];
+        if (!make_map(&p.a_load[r], base + a_off, K_r, M, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map(&p.b_load[r], base + b_off, N, K_r, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map(&p.out_store[r], base + out_off, N, Mb, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+            return OPW_ERR_CUDA;
+    }
+    p.flags = sig->flags;
+    p.status = sig->status;
+    p.trace = o.trace_dev;
+    p.epoch = epoch;
+    p.timeout_ns = o.timeout_ns != 0 ? o.timeout_ns : kDefaultTimeoutNs;
+    p.R = R;
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K_r = static_cast<int32_t>(K_r);
+    p.Mb = static_cast<int32_t>(Mb);
+    p.T_M = static_cast<int32_t>(M / BM);
+    p.T_N = static_cast<int32_t>((N + BN - 1) / BN);
+    p.T_fm = static_cast<int32_t>(Mb / 128);
+    p.T_fn = static_cast<int32_t>((N + 127) / 128);
+    if (launch_gemm_rs(p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return OPW_ERR_CUDA;
+    sig->epoch_last = epoch;
+    return OPW_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+// Internal interface between the C-ABI host code (opw_host.cu) and the
+// kernels: parameter blocks passed by value as __grid_constant__ and the
+// launch entry points.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/opw.h"
+
+namespace opw {
+
+// GEMM tiling shared by both kernels (one CTA per SM, tcgen05 cta_group::1).
+constexpr int BM = 128;       // rows per output tile = TMEM lanes
+constexpr int BN = 256;       // columns per output tile = fp32 TMEM columns per accumulator
+constexpr int BK = 64;        // K per pipeline stage = one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;    // K per tcgen05.mma (kind::f16)
+constexpr int STAGES = 4;     // A/B shared-memory ring depth
+constexpr int TILE_Q = 4;     // depth of the tile-id queue (loader -> MMA, epilogue)
+
+constexpr int A_STAGE_BYTES = BM * BK * 2;       // 16 KiB
+constexpr int B_CHUNK_BYTES = BK * 64 * 2;       // 8 KiB: 64 K-rows x 64 N-columns
+constexpr int B_STAGE_BYTES = BK * BN * 2;       // 32 KiB: 4 chunks
+constexpr int EPI_WARP_BYTES = 32 * 64 * 2;      // 4 KiB: 32 rows x 64 columns bf16
+constexpr int GATHER_SUB_ROWS = 32;              // producer copies a flag tile 32 rows at a time
+constexpr int GATHER_BUF_BYTES = GATHER_SUB_ROWS * 128 * 2;  // 8 KiB (flag tile <= 128 wide)
+
+// Counter words in the signal object after the flags: per-rank publish
+// counts, then the tile-claim counter of the dynamic schedule.
+constexpr int CTR_RANK_DONE = 0;
+constexpr int CTR_CLAIM = OPW_MAX_RANKS;
+constexpr int CTR_WORDS = OPW_MAX_RANKS + 8;
+
+// Error-site tags written to status[2] when an on-chip wait times out.
+enum WaitSite : int32_t {
+    SITE_LOADER_EMPTY = 1001,
+    SITE_MMA_FULL = 1002,
+    SITE_MMA_TMEM_EMPTY = 1003,
+    SITE_EPI_TMEM_FULL = 1004,
+    SITE_TILE_QUEUE = 1005,
+    SITE_GATHER_LOAD = 1006,
+    SITE_DRAIN = 1007,
+    SITE_SKEW_ORDER = 1008,
+    SITE_SERIAL = 1009,
+};
+
+struct AgParams {
+    CUtensorMap shard[OPW_MAX_RANKS];  // A_r [M_r, K], box {ft, 32}, no swizzle (producer load)
+    CUtensorMap g_store;               // G [M, K], box {ft, 32}, no swizzle (producer store)
+    CUtensorMap g_load;                // G [M, K], box {64, 128}, 128B swizzle (consumer A)
+    CUtensorMap b_load;                // B [K, N], box {64, 64}, 128B swizzle (consumer B)
+    CUtensorMap c_store;               // C [M, N], box {64, 32}, 128B swizzle (epilogue)
+    int64_t* flags;
+    int32_t* status;
+    unsigned long long* counters;
+    uint64_t* trace;
+    uint64_t epoch;
+    uint64_t timeout_ns;
+    uint64_t claim_base;      // claim-counter value before this launch
+    int32_t R, M_r, M, N, K;
+    int32_t ft;               // flag tile edge (64 or 128)
+    int32_t T_mr, T_k;        // flag tiles per rank along M, along K
+    int32_t T_M, T_N;         // output tiles
+    int32_t role, sync_mode, schedule;
+    int32_t has_perm, has_delay;
+    int32_t fault_kind, fault_arg;
+    int32_t perm[OPW_MAX_RANKS];
+    uint32_t delay_ns[OPW_MAX_RANKS];
+    // rank r's publish counter once every tile of this epoch is published
+    uint64_t rank_target[OPW_MAX_RANKS];
+};
+
+struct RsParams {
+    CUtensorMap a_load[OPW_MAX_RANKS];  // A_r [M, K_r], box {64, 128}, 128B swizzle
+    CUtensorMap b_load[OPW_MAX_RANKS];  // B_r [K_r, N], box {64, 64}, 128B swizzle
+    CUtensorMap out_store[OPW_MAX_RANKS];  // out_j [M/R, N], box {64, 32}, 128B swizzle
+    int64_t* flags;
+    int32_t* status;
+    uint64_t* trace;
+    uint64_t epoch;
+    uint64_t timeout_ns;
+    int32_t R, M, N, K_r, Mb;
+    int32_t T_M, T_N;
+    int32_t T_fm, T_fn;       // 128x128 flag tiles per rank block along M, along N
+};
+
+// Shared memory each kernel asks for (dynamic, includes 1 KiB alignment slack).
+size_t ag_smem_bytes();
+size_t rs_smem_bytes();
+
+// Launch helpers (cooperative launch so every CTA is co-resident).
+cudaError_t launch_ag_gemm(const AgParams& p, int grid, cudaStream_t s);
+cudaError_t launch_gemm_rs(const RsParams& p, int grid, cudaStream_t s);
+
+}  // namespace opw

@@ -1,0 +1,247 @@
+"""AllGather -> GEMM on the GPU against the CPU oracle, through the C ABI.
+
+Bit-exact: the gathered buffer G, every flag (== epoch) and the identity /
+all-ones special cases.  Floating point C: rel-Frobenius <= 1e-3 and
+per-element <= 1e-2 * max|C_ref| against the oracle's fp64 result rounded to
+bf16.  Sizes span several tiles and ragged edges; the tensor-parallel
+configuration is checked on sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from overlap_producer_warps_gb300 import inputs
+from tests.helpers import AgProblem, assert_gemm_close, host_bits, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from overlap_producer_warps_gb300 import api as _api
+    _api.lib()
+    return _api
+
+
+def _cfg(R, M_r, K, N, dist="normal", scale=0.5):
+    return dict(R=R, M_r=M_r, K=K, N=N, dist=dist, scale=scale)
+
+
+def _run_and_check(api, d, epoch_runs=1, opts_fn=None, full=True):
+    prob = AgProblem(d)
+    F = api.ag_num_flags(prob.R, prob.M_r, prob.K)
+    sig = api.Signal(F)
+    for i in range(epoch_runs):
+        e = sig.next_epoch()
+        prob.run(api, sig, e, opts_fn(i) if opts_fn else None)
+        st = sig.status()
+        assert st[0] == api.OK, st
+        flags = sig.flags().cpu().numpy()
+        assert np.array_equal(flags, oracle.expected_flags(F, e)), f"flags after epoch {e}"
+    G_ref, C_ref = prob.oracle_full() if full else (None, None)
+    if full:
+        assert np.array_equal(host_bits(prob.G), G_ref), "gathered buffer differs"
+        assert_gemm_close(host_bits(prob.C), C_ref)
+    sig.close()
+    return prob
+
+
+def test_tiny_config(api):
+    """R=2, 64x128 shards, B 128x128, 64x64 flag tiles, uniform[-1,1] seed 0, epoch 1."""
+    cfg = inputs.CONFIGS["ag_tiny"]
+    d = inputs.ag_inputs(cfg, seed=0)
+    assert api.ag_flag_tile(cfg["M_r"], cfg["K"]) == cfg["flag_tile"]
+    assert api.ag_num_flags(cfg["R"], cfg["M_r"], cfg["K"]) == 4
+    _run_and_check(api, d)
+
+
+def test_identity_b_is_bit_exact_gather(api):
+    # B = I makes C = bf16(G) exactly: pins the A operand path bit for bit.
+    R, M_r, K = 2, 128, 256
+    d = inputs.ag_inputs(_cfg(R, M_r, K, K), seed=3)
+    d["B"] = np.where(np.eye(K, dtype=bool), np.uint16(0x3F80), np.uint16(0)).astype(np.uint16)
+    prob = AgProblem(d)
+    sig = api.Signal(api.ag_num_flags(R, M_r, K))
+    prob.run(api, sig, sig.next_epoch())
+    assert sig.status()[0] == api.OK
+    G = host_bits(prob.G)
+    assert np.array_equal(host_bits(prob.C), G)
+    assert np.array_equal(G, oracle.allgather(d["heap"], d["rank_off"], R, d["a_off"], M_r, K))
+
+
+def test_one_hot_a_picks_rows_of_b(api):
+    # A one-hot (row i selects row perm[i] of B) pins the B operand layout.
+    R, M_r, K, N = 2, 128, 256, 512
+    d = inputs.ag_inputs(_cfg(R, M_r, K, N), seed=4)
+    rng = np.random.default_rng(4)
+    for r in range(R):
+        A = np.zeros((M_r, K), dtype=np.uint16)
+        A[np.arange(M_r), rng.integers(0, K, M_r)] = 0x3F80
+        o = int(d["rank_off"][r])
+        d["heap"][o:o + A.nbytes] = A.view(np.uint8).reshape(-1)
+    prob = AgProblem(d)
+    sig = api.Signal(api.ag_num_flags(R, M_r, K))
+    prob.run(api, sig, sig.next_epoch())
+    assert sig.status()[0] == api.OK
+    G = oracle.allgather(d["heap"], d["rank_off"], R, d["a_off"], M_r, K)
+    picks = np.argmax(G, axis=1)
+    assert np.array_equal(host_bits(prob.C), d["B"][picks])
+
+
+def test_all_ones_gives_k(api):
+    R, M_r, K, N = 2, 128, 384, 256
+    d = inputs.ag_inputs(_cfg(R, M_r, K, N), seed=5)
+    for r in range(R):
+        o = int(d["rank_off"][r])
+        d["heap"][o:o + M_r * K * 2] = np.full(M_r * K, 0x3F80, dtype=np.uint16).view(np.uint8)
+    d["B"] = np.full((K, N), 0x3F80, dtype=np.uint16)
+    prob = AgProblem(d)
+    sig = api.Signal(api.ag_num_flags(R, M_r, K))
+    prob.run(api, sig, sig.next_epoch())
+    assert sig.status()[0] == api.OK
+    assert np.all(oracle.bf16_to_f64(host_bits(prob.C)) == float(K))
+
+
+@pytest.mark.parametrize("R,M_r,K,N,order", [
+    (3, 64, 192, 200, (2, 0, 1)),      # flag tile 64, GEMM tiles straddle ranks, ragged N
+    (4, 256, 512, 776, (1, 3, 0, 2)),  # flag tile 128, ragged N, permuted rank table
+    (1, 128, 128, 8, None),            # single rank, narrowest N
+    (8, 128, 1024, 512, None),         # eight ranks, several k-blocks per flag
+    (5, 192, 320, 264, (4, 3, 2, 1, 0)),  # ragged M (960 rows) and N
+])
+def test_shapes(api, R, M_r, K, N, order):
+    d = inputs.ag_inputs(_cfg(R, M_r, K, N), seed=R * 7 + K, slot_order=order)
+    _run_and_check(api, d)
+
+
+def test_epochs_reused_without_reset(api):
+    """20 launches on one signal object: flags == e after each (TP-style epochs 1..20)."""
+    d = inputs.ag_inputs(_cfg(4, 128, 256, 512), seed=9)
+    _run_and_check(api, d, epoch_runs=20)
+
+
+def test_serial_mode_matches_overlap_bit_for_bit(api):
+    d = inputs.ag_inputs(_cfg(4, 256, 512, 512), seed=10)
+    p1 = _run_and_check(api, d)
+    p2 = _run_and_check(api, d, opts_fn=lambda i: api.make_opts(sync_mode=api.SYNC_SERIAL))
+    assert np.array_equal(host_bits(p1.C), host_bits(p2.C))
+
+
+def test_ready_schedule_matches_swizzle_bit_for_bit(api):
+    d = inputs.ag_inputs(_cfg(4, 256, 512, 768), seed=11)
+    p1 = _run_and_check(api, d)
+    p2 = _run_and_check(api, d, epoch_runs=3,
+                        opts_fn=lambda i: api.make_opts(schedule=api.SCHED_READY))
+    assert np.array_equal(host_bits(p1.C), host_bits(p2.C))
+
+
+def test_producer_then_consumer_roles(api):
+    d = inputs.ag_inputs(_cfg(4, 128, 384, 512), seed=12)
+    prob = AgProblem(d)
+    F = api.ag_num_flags(4, 128, 384)
+    sig = api.Signal(F)
+    e = sig.next_epoch()
+    prob.run(api, sig, e, api.make_opts(role=api.ROLE_PRODUCER))
+    assert sig.status()[0] == api.OK
+    assert np.all(sig.flags().cpu().numpy() == e)
+    assert sig.next_epoch() == e + 1
+    prob.run(api, sig, e, api.make_opts(role=api.ROLE_CONSUMER))
+    assert sig.status()[0] == api.OK
+    G_ref, C_ref = prob.oracle_full()
+    assert np.array_equal(host_bits(prob.G), G_ref)
+    assert_gemm_close(host_bits(prob.C), C_ref)
+
+
+def test_fewer_ctas_than_sms(api):
+    d = inputs.ag_inputs(_cfg(2, 256, 256, 512), seed=13)
+    _run_and_check(api, d, opts_fn=lambda i: api.make_opts(num_ctas=5))
+
+
+def _trace_views(api, prob, trace, grid):
+    F = api.ag_num_flags(prob.R, prob.M_r, prob.K)
+    T = ((prob.M + 127) // 128) * ((prob.N + 255) // 256)
+    t = trace.cpu().numpy().view(np.uint64)
+    return dict(publish=t[:F], consume=t[F:2 * F], tile=t[2 * F:2 * F + T],
+                tile_start=t[2 * F + T:2 * F + 2 * T], cta_start=t[2 * F + 2 * T:2 * F + 2 * T + grid],
+                F=F, T=T)
+
+
+def test_trace_publish_before_consume_and_swizzle_order(api):
+    R, M_r, K, N = 4, 256, 512, 1024
+    d = inputs.ag_inputs(_cfg(R, M_r, K, N), seed=14)
+    prob = AgProblem(d)
+    sig = api.Signal(api.ag_num_flags(R, M_r, K))
+    words = api.ag_trace_words(R, M_r, N, K)
+    trace = torch.full((words,), -1, dtype=torch.int64, device="cuda")
+    grid = 6
+    prob.run(api, sig, sig.next_epoch(), api.make_opts(trace=trace, num_ctas=grid))
+    assert sig.status()[0] == api.OK
+    v = _trace_views(api, prob, trace, grid)
+    # every tile published, and no consumer acquired a tile before its publish
+    assert np.all(v["publish"] > 0) and np.all(v["consume"] != np.uint64(2 ** 64 - 1))
+    assert np.all(v["publish"] <= v["consume"])
+    # each CTA visited its tiles in the oracle's swizzled order
+    T_M, T_N = prob.M // 128, (N + 255) // 256
+    cta = (v["tile"] >> np.uint64(32)).astype(np.int64)
+    pos = (v["tile"] & np.uint64(0xFFFFFFFF)).astype(np.int64)
+    for c in range(grid):
+        mine = np.nonzero(cta == c)[0]
+        got = mine[np.argsort(pos[mine])]
+        assert list(got) == list(oracle.consumer_order(T_M, T_N, R, grid, c)), c
+    G_ref, C_ref = prob.oracle_full()
+    assert_gemm_close(host_bits(prob.C), C_ref)
+
+
+def test_skewed_readiness_order_and_delays(api):
+    R, M_r, K, N = 8, 128, 512, 512
+    d = inputs.ag_inputs(_cfg(R, M_r, K, N), seed=15)
+    perm, delay = inputs.skew_schedule(0, R)
+    prob = AgProblem(d)
+    sig = api.Signal(api.ag_num_flags(R, M_r, K))
+    words = api.ag_trace_words(R, M_r, N, K)
+    trace = torch.full((words,), -1, dtype=torch.int64, device="cuda")
+    for _ in range(2):
+        trace.fill_(-1)
+        prob.run(api, sig, sig.next_epoch(),
+                 api.make_opts(publish_perm=perm, delay_ns=delay, trace=trace))
+        assert sig.status()[0] == api.OK
+        v = _trace_views(api, prob, trace, torch.cuda.get_device_properties(0).multi_processor_count)
+        per_rank = v["F"] // R
+        pub = v["publish"].reshape(R, per_rank)
+        for i in range(1, R):
+            assert pub[perm[i - 1]].max() <= pub[perm[i]].min(), f"rank {perm[i]} before {perm[i - 1]}"
+        t0 = v["cta_start"].min()
+        for r in range(R):
+            assert pub[r].min() >= t0 + delay[r], f"rank {r} published before its delay"
+        assert np.all(v["publish"] <= v["consume"])
+    G_ref, C_ref = prob.oracle_full()
+    assert np.array_equal(host_bits(prob.G), G_ref)
+    assert_gemm_close(host_bits(prob.C), C_ref)
+
+
+@pytest.mark.parametrize("name", ["ag_tp", "ag_mlp", "ag_skew"])
+def test_full_size_configs_sampled(api, name):
+    """The benchmark's workloads at full size, in its launch configuration; sampled rows."""
+    cfg = inputs.CONFIGS[name]
+    d = inputs.ag_inputs(cfg, seed=0)
+    prob = AgProblem(d)
+    sig = api.Signal(api.ag_num_flags(prob.R, prob.M_r, prob.K))
+    opts = None
+    if cfg.get("skew"):
+        perm, delay = inputs.skew_schedule(0, prob.R)
+        opts = api.make_opts(publish_perm=perm, delay_ns=delay)
+    for _ in range(2):
+        prob.run(api, sig, sig.next_epoch(), opts)
+        assert sig.status()[0] == api.OK
+    assert np.all(sig.flags().cpu().numpy() == 2)
+    # gathered buffer bit-exact (full), C on sampled rows of every row tile
+    G = host_bits(prob.G)
+    assert np.array_equal(G, oracle.allgather(d["heap"], d["rank_off"], prob.R, d["a_off"],
+                                              prob.M_r, prob.K))
+    per_tile = 1 if prob.M * prob.N * prob.K < 2 ** 38 else 0
+    rows = sample_rows(prob.M, 128 if per_tile else 512, per_tile, seed=1)
+    C = host_bits(prob.C)
+    assert_gemm_close(C[rows], prob.oracle_rows(rows), what=f"{name} sampled C")

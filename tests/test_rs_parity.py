@@ -1,0 +1,110 @@
+"""GEMM -> ReduceScatter on the GPU against the CPU oracle, through the C ABI.
+
+Each rank j's output block must match rows [j*M/R, (j+1)*M/R) of the oracle's
+fp64 sum of partials (rounded to bf16) within rel-Frobenius 1e-3 and
+per-element 1e-2*max|ref|; every flag must equal the epoch; repeated runs
+must be bit-identical (fixed-order fp32 reduction).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from overlap_producer_warps_gb300 import inputs
+from tests.helpers import RsProblem, assert_gemm_close, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from overlap_producer_warps_gb300 import api as _api
+    _api.lib()
+    return _api
+
+
+def _cfg(R, M, K_r, N, scale=0.5):
+    return dict(R=R, M=M, K_r=K_r, N=N, dist="normal", scale=scale)
+
+
+def _check_all(api, prob, rows=None):
+    R, Mb = prob.R, prob.Mb
+    if rows is None:
+        rows = np.arange(prob.M)
+    S = prob.oracle_rows(rows)
+    for j in range(R):
+        sel = (rows >= j * Mb) & (rows < (j + 1) * Mb)
+        if not np.any(sel):
+            continue
+        got = prob.out_bits(j)[rows[sel] - j * Mb]
+        assert_gemm_close(got, S[sel], what=f"out_{j}")
+
+
+@pytest.mark.parametrize("R,M,K_r,N,order", [
+    (2, 256, 128, 256, None),
+    (3, 384, 200, 328, (2, 0, 1)),     # ragged K_r and N, permuted rank table
+    (8, 1024, 64, 512, None),
+    (1, 256, 320, 264, None),          # single rank: plain GEMM
+    (4, 1024, 448, 1024, (3, 1, 2, 0)),
+])
+def test_shapes(api, R, M, K_r, N, order):
+    d = inputs.rs_inputs(_cfg(R, M, K_r, N), seed=R * 5 + K_r, slot_order=order)
+    prob = RsProblem(d)
+    F = api.rs_num_flags(R, M, N)
+    sig = api.Signal(F)
+    e = sig.next_epoch()
+    prob.run(api, sig, e)
+    st = sig.status()
+    assert st[0] == api.OK, st
+    assert np.array_equal(sig.flags().cpu().numpy(), oracle.expected_flags(F, e))
+    _check_all(api, prob)
+
+
+def test_deterministic_and_epochs(api):
+    R, M, K_r, N = 4, 512, 256, 512
+    d = inputs.rs_inputs(_cfg(R, M, K_r, N), seed=31)
+    prob = RsProblem(d)
+    F = api.rs_num_flags(R, M, N)
+    sig = api.Signal(F)
+    outs = []
+    for _ in range(5):
+        e = sig.next_epoch()
+        prob.run(api, sig, e)
+        assert sig.status()[0] == api.OK
+        assert np.all(sig.flags().cpu().numpy() == e)
+        outs.append(np.concatenate([prob.out_bits(j) for j in range(R)]))
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    _check_all(api, prob)
+
+
+def test_only_output_regions_are_written(api):
+    R, M, K_r, N = 2, 256, 128, 256
+    d = inputs.rs_inputs(_cfg(R, M, K_r, N), seed=32)
+    prob = RsProblem(d)
+    before = prob.heap.cpu().numpy().copy()
+    sig = api.Signal(api.rs_num_flags(R, M, N))
+    prob.run(api, sig, sig.next_epoch())
+    assert sig.status()[0] == api.OK
+    after = prob.heap.cpu().numpy()
+    mask = np.ones(before.size, dtype=bool)
+    for j in range(R):
+        o = int(prob.rank_off[j]) + d["out_off"]
+        mask[o:o + prob.Mb * N * 2] = False
+    assert np.array_equal(before[mask], after[mask])
+
+
+def test_full_size_tp_sampled(api):
+    """GEMM-RS TP layer at full size (R=8, A_r 8192x1792, B_r 1792x4096), sampled rows."""
+    cfg = inputs.CONFIGS["rs_tp"]
+    d = inputs.rs_inputs(cfg, seed=0)
+    prob = RsProblem(d)
+    sig = api.Signal(api.rs_num_flags(prob.R, prob.M, prob.N))
+    for _ in range(2):
+        prob.run(api, sig, sig.next_epoch())
+        assert sig.status()[0] == api.OK
+    assert np.all(sig.flags().cpu().numpy() == 2)
+    rows = sample_rows(prob.M, 128, 1, seed=2)
+    _check_all(api, prob, rows)
