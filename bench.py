@@ -127,6 +127,21 @@ def kernel_traffic(name: str):
     return ent["dram_bytes_per_launch"] if h == ent.get("source_sha256_16") else None
 
 
+def reduce_max(x: float, dist, device) -> float:
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_rank_step: float, ms_per_step_max: float) -> float:
+    """Weak scaling: every rank does the same work; time is the slowest rank's."""
+    return world * flops_per_rank_step / (ms_per_step_max * 1e-3) / 1e12
+
+
 def source_hash(fname: str) -> str:
     src = os.path.join(ROOT, "overlap_producer_warps_gb300", "csrc", fname)
     return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
@@ -426,13 +441,9 @@ def run_ours(args, rank, world, dist):
     ms_total = start.elapsed_time(end)
     ag_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     rs_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    t_step = ms_total / args.steps
-    if dist is not None:
-        t = torch.tensor([t_step], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step = float(t.item())
+    t_step = reduce_max(ms_total / args.steps, dist, "cuda")
     flops_step = w.flops_ag + w.flops_rs
-    value = world * flops_step / (t_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops_step, t_step)
 
     # ---- end to end through the public API with host buffers
     a, r = w.ag_d, w.rs_d
@@ -476,12 +487,8 @@ def run_ours(args, rank, world, dist):
     e1.record(stream)
     torch.cuda.synchronize()
     w.check()
-    t_e2e = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([t_e2e], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_e2e = float(t.item())
-    e2e = {"value": world * flops_step / (t_e2e * 1e-3) / 1e12, "unit": UNIT,
+    t_e2e = reduce_max(e0.elapsed_time(e1) / args.steps, dist, "cuda")
+    e2e = {"value": whole_job_tflops(world, flops_step, t_e2e), "unit": UNIT,
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
            "ms_per_step": t_e2e}
 
