@@ -230,6 +230,46 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
                        const void* B_dev, void* G_dev, void* C_dev, opw_signal* sig,
                        uint64_t epoch, const opw_opts* opts, void* stream);
 
+/* ------------------------------------------- AG-GEMM without allocation */
+
+/*
+ * The pages have no counterpart to this call: it exists for callers that
+ * cannot allocate device memory.  opw_ag_gemm needs a signal object, and
+ * opw_signal_alloc calls cudaMalloc.  Some callers cannot: code that runs
+ * inside a framework owning all device memory through its own pool (a raw
+ * allocation bypasses its accounting or fails against its cap), and
+ * latency-critical serving loops that cannot take cudaMalloc's implicit
+ * device synchronisation.  This variant computes the same G and C as
+ * opw_ag_gemm and calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Scratch: the per-tile flags and counters live in one fixed array compiled
+ * into the library, sized for OPW_NOALLOC_MAX_FLAGS flag tiles (about
+ * 512 KiB).  Every GPU that loads the library holds it until the process
+ * exits.  A call whose opw_ag_num_flags(R, M_r, K) exceeds the maximum is
+ * rejected with OPW_ERR_UNSUPPORTED_SHAPE before anything is launched.
+ *
+ * Sharing: every call on a device uses the same array.  Each call clears the
+ * flags and counters it needs (and *status_dev) on `stream`, then publishes
+ * epoch 1.  Calls that overlap on the GPU (other streams, other threads)
+ * therefore race and give wrong results: serialise them.
+ *
+ * Set-up: the first call on a device, with that device current, looks up
+ * the array's device address.  Make that first call before any stream
+ * capture.
+ *
+ *   status_dev : device int32[4], 16-byte aligned, written by the call:
+ *                [0] status (OPW_OK or a device-side error such as
+ *                OPW_ERR_TIMEOUT), [1] rank, [2] flag slot.  The caller reads
+ *                it after synchronising the stream.
+ *   opts       : as for opw_ag_gemm, except role must be OPW_ROLE_FUSED.
+ * All other arguments, shapes, alignment rules and errors are those of
+ * opw_ag_gemm (there is no signal object and no epoch argument).
+ */
+#define OPW_NOALLOC_MAX_FLAGS 65536
+opw_status opw_ag_gemm_noalloc(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t N,
+                               int64_t K, const void* B_dev, void* G_dev, void* C_dev,
+                               int32_t* status_dev, const opw_opts* opts, void* stream);
+
 /* ---------------------------------------------------------------- GEMM-RS */
 
 /* Flag slots for GEMM-RS outputs: 128x128 tiles of each rank's [M/R, N]

@@ -71,6 +71,9 @@ SIGNATURES = {
     "opw_ag_gemm": (ctypes.c_int32, [ctypes.POINTER(Symm), ctypes.c_size_t, ctypes.c_int64,
                                      ctypes.c_int64, ctypes.c_int64, _vp, _vp, _vp, _vp,
                                      ctypes.c_uint64, ctypes.POINTER(Opts), _vp]),
+    "opw_ag_gemm_noalloc": (ctypes.c_int32, [ctypes.POINTER(Symm), ctypes.c_size_t,
+                                             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _vp,
+                                             _vp, _vp, _vp, ctypes.POINTER(Opts), _vp]),
     "opw_rs_num_flags": (ctypes.c_int64, [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64]),
     "opw_gemm_rs": (ctypes.c_int32, [ctypes.POINTER(Symm), ctypes.c_size_t, ctypes.c_size_t,
                                      ctypes.c_size_t, ctypes.c_int64, ctypes.c_int64,
@@ -247,6 +250,26 @@ def ag_gemm(heap, rank_off, a_off, M_r, N, K, B, G, C, sig: Signal, epoch, opts=
     """AllGather -> GEMM (see opw_ag_gemm).  Asynchronous on `stream`."""
     _check(ag_gemm_status(heap, rank_off, a_off, M_r, N, K, B, G, C, sig, epoch, opts, stream),
            "opw_ag_gemm")
+
+
+NOALLOC_MAX_FLAGS = 65536
+
+
+def ag_gemm_noalloc_status(heap, rank_off, a_off, M_r, N, K, B, G, C, status, opts=None,
+                           stream=None) -> int:
+    """opw_ag_gemm_noalloc, for callers that cannot allocate device memory.
+
+    Same result as ag_gemm, with its scratch in a fixed array inside the
+    library instead of a signal object.  `status` is a caller-owned device
+    int32 tensor of 4 elements that receives the device-side status.
+    Returns the host-side status code.
+    """
+    s = _symm(heap, rank_off)
+    return int(lib().opw_ag_gemm_noalloc(ctypes.byref(s), int(a_off), int(M_r), int(N), int(K),
+                                         B.data_ptr(), G.data_ptr(), C.data_ptr(),
+                                         status.data_ptr(),
+                                         ctypes.byref(opts) if opts is not None else None,
+                                         _stream_ptr(stream)))
 
 
 def gemm_rs_status(heap, rank_off, a_off, b_off, out_off, M, N, K_r, sig: Signal, epoch,
