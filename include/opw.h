@@ -139,10 +139,12 @@ typedef struct {
                                 (the "test with barrier sync first" debug mode
                                 of "Triton-distributed Semantics", Best Practices 8) */
 
-#define OPW_SCHED_SWIZZLE 0  /* static: CTA c starts on home rank c mod R and
+#define OPW_SCHED_READY   0  /* dynamic (default): CTAs claim output tiles from a
+                                device counter in the order their rows are
+                                published, so every consumer starts on the tiles
+                                that are ready first */
+#define OPW_SCHED_SWIZZLE 1  /* static: CTA c starts on home rank c mod R and
                                 rotates ("Threadblock Swizzling") */
-#define OPW_SCHED_READY   1  /* dynamic: CTAs claim output tiles from a device
-                                counter in the order their rows are published */
 
 #define OPW_ROLE_FUSED    0  /* producer warps and consumer warps together */
 #define OPW_ROLE_PRODUCER 1  /* only the gather + publish (for overlap timing) */
@@ -191,7 +193,8 @@ int64_t opw_ag_num_flags(int32_t R, int64_t M_r, int64_t K);
  *                     succeeded (atomicMin; the caller fills this range
  *                     with all-ones bits before the launch)
  *   [2F, 2F+T)        per output tile: (cta << 32) | visit position
- *   [2F+T, 2F+2T)     per output tile: time its first A load was issued
+ *   [2F+T, 2F+2T)     per output tile: time the loader began it (before its
+ *                     first flag acquire)
  *   [2F+2T, 2F+2T+G)  per CTA: start time
  * with F = opw_ag_num_flags(), T = ceil(M/128)*ceil(N/256), G = grid size
  * (at most OPW_TRACE_MAX_CTAS words are reserved).

@@ -27,7 +27,7 @@ ERR_FLAG_PROTOCOL = 7
 ERR_NOT_READY = 8
 
 SYNC_OVERLAP, SYNC_SERIAL = 0, 1
-SCHED_SWIZZLE, SCHED_READY = 0, 1
+SCHED_READY, SCHED_SWIZZLE = 0, 1
 ROLE_FUSED, ROLE_PRODUCER, ROLE_CONSUMER = 0, 1, 2
 FAULT_NONE, FAULT_DROP_TILE, FAULT_STALE_EPOCH = 0, 1, 2
 MAX_RANKS = 8
@@ -180,7 +180,7 @@ class Signal:
             pass
 
 
-def make_opts(timeout_ns=0, sync_mode=SYNC_OVERLAP, schedule=SCHED_SWIZZLE, role=ROLE_FUSED,
+def make_opts(timeout_ns=0, sync_mode=SYNC_OVERLAP, schedule=SCHED_READY, role=ROLE_FUSED,
               num_ctas=0, publish_perm=None, delay_ns=None, trace=None, fault_kind=FAULT_NONE,
               fault_arg=0):
     """Build an Opts struct; array arguments are kept alive on the struct."""

@@ -11,6 +11,9 @@
 //   warp 0     loader: acquires the flags of the A tiles a k-block needs, then
 //              TMA-loads the A tile from the gathered buffer G and the B tile
 //              into a 4-stage shared-memory ring.  Owns the tile schedule.
+//              Flag acquisition sits outside the k-block loop, and the next
+//              tile's flags are looked at while the current tile's last
+//              stages load, so the loop itself is a plain GEMM pipeline.
 //   warp 1     MMA: one thread issues tcgen05.mma (bf16 x bf16 -> fp32) into a
 //              double-buffered TMEM accumulator (2 x 128 lanes x 256 columns).
 //   warp 2     gather producer: TMA-copies flag tiles of A_r into G through
@@ -144,7 +147,110 @@ __device__ __forceinline__ int poll_flags(const AgParams& p, int base0, int base
     return n;
 }
 
+// Acquire at least one more flag column of the tile (bounded wait): on
+// return ready_kt has advanced past every column already published.
+__device__ __noinline__ bool acquire_flags(const AgParams& p, const ErrCtx& ec, int base0,
+                                           int base1, int& ready_kt)
+{
+    const uint32_t lane = lane_id();
+    uint64_t t0 = 0;
+    for (uint32_t spins = 0;; ++spins) {
+        const int n = poll_flags(p, base0, base1, ready_kt);
+        if (n > 0) {
+            ready_kt += n;
+            // take any further columns that are already published, without waiting
+            while (ready_kt < p.T_k) {
+                const int more = poll_flags(p, base0, base1, ready_kt);
+                if (more == 0) break;
+                ready_kt += more;
+            }
+            return true;
+        }
+        if (spins == 0) t0 = globaltimer();
+        __nanosleep(128);
+        if ((spins & 7u) == 7u) {
+            if (aborted(ec)) return false;
+            if (globaltimer() - t0 > ec.timeout_ns) {
+                if (lane == 0) {
+                    const int slot = base0 + ready_kt;  // first missing slot
+                    raise_error(ec, OPW_ERR_TIMEOUT, slot / (p.T_mr * p.T_k), slot);
+                }
+                return false;
+            }
+        }
+    }
+}
+
+// How many leading flag columns of a tile are already published (no wait).
+__device__ __noinline__ int peek_flags(const AgParams& p, int base0, int base1)
+{
+    int ready_kt = 0;
+    while (ready_kt < p.T_k) {
+        const int n = poll_flags(p, base0, base1, ready_kt);
+        if (n == 0) break;
+        ready_kt += n;
+    }
+    return ready_kt;
+}
+
 // ------------------------------------------------------------------ loader
+
+// Flag rows covered by output rows [m0, m0 + BM): one for 128-row flag tiles,
+// two for 64-row ones (base1 = -1 when there is no second row).
+__device__ __forceinline__ void flag_rows(const AgParams& p, int m0, int& base0, int& base1)
+{
+    const int r = m0 / p.M_r;
+    const int mt = (m0 - r * p.M_r) / p.ft;
+    base0 = (r * p.T_mr + mt) * p.T_k;
+    base1 = -1;
+    if (p.ft < BM && m0 + p.ft < p.M) {
+        const int g = m0 + p.ft;
+        const int r1 = g / p.M_r;
+        const int mt1 = (g - r1 * p.M_r) / p.ft;
+        base1 = (r1 * p.T_mr + mt1) * p.T_k;
+    }
+}
+
+struct LoaderRing {
+    uint32_t stage = 0, sphase = 0, filled = 0, last_par = 0;
+};
+
+// Issue the TMA loads of k-blocks [kb0, kb1) of tile (m0, n0): the plain
+// GEMM pipeline, with nothing else in the loop.
+__device__ __forceinline__ bool issue_kblocks(const AgParams& p, uint8_t* smem, AgCtrl* ctrl,
+                                              const ErrCtx& ec, LoaderRing& rg, int m0, int n0,
+                                              int kb0, int kb1)
+{
+    const uint32_t lane = lane_id();
+    for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wait_bar(&ctrl->empty[rg.stage], rg.sphase ^ 1u, ec, SITE_LOADER_EMPTY)) return false;
+        if (lane == 0) {
+            uint64_t* fb = &ctrl->full[rg.stage];
+            mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
+            tma_load_2d(smem + OFF_A + rg.stage * A_STAGE_BYTES, &p.g_load, fb, kb * BK, m0);
+            uint8_t* bs = smem + OFF_B + rg.stage * B_STAGE_BYTES;
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(bs + j * B_CHUNK_BYTES, &p.b_load, fb, n0 + 64 * j, kb * BK);
+        }
+        __syncwarp();
+        rg.filled |= 1u << rg.stage;
+        rg.last_par = (rg.last_par & ~(1u << rg.stage)) | (rg.sphase << rg.stage);
+        if (++rg.stage == STAGES) { rg.stage = 0; rg.sphase ^= 1u; }
+    }
+    return true;
+}
+
+// consume_token: order the flag acquires (made by every lane of this warp)
+// before any later async-proxy read issued by lane 0.
+__device__ __forceinline__ void consume_token()
+{
+    if (lane_id() == 0) {
+        fence_acq_rel_gpu();
+        fence_async_global();
+    }
+    __syncwarp();
+}
 
 __device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const ErrCtx& ec)
 {
@@ -153,6 +259,7 @@ __device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
     const int c = static_cast<int>(blockIdx.x);
     const int T = p.T_M * p.T_N;
     const int KB = p.K / BK;
+    const int kb_per_col = p.ft / BK;  // k-blocks per flag column
 
     // Static schedule: this CTA owns tiles q = c + i*G; it starts at the first
     // one in its home rank's rows (h*tiles_per_pe row tiles down) and wraps.
@@ -162,23 +269,27 @@ __device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
     int i0 = start_q <= c ? 0 : static_cast<int>((start_q - c + G - 1) / G);
     if (i0 >= n_mine) i0 = 0;
 
-    uint32_t stage = 0, sphase = 0, tq = 0, tqphase = 0;
-    uint32_t filled = 0, last_par = 0;
-    bool ok = true;
-    bool serial_pending = (p.sync_mode == OPW_SYNC_SERIAL);
-
-    for (int s = 0; ok; ++s) {
-        int q;
+    // Tile at visit position s (-1 = none).  The dynamic schedule claims from
+    // the device counter; tiles come out in the order their rows are published.
+    auto tile_at = [&](int s) -> int {
         if (p.schedule == OPW_SCHED_READY) {
             long long idx = 0;
             if (lane == 0)
                 idx = static_cast<long long>(atomicAdd(p.counters + CTR_CLAIM, 1ull) - p.claim_base);
             idx = __shfl_sync(0xffffffffu, idx, 0);
-            q = idx < T ? ready_tile(p, static_cast<int>(idx)) : -1;
-        } else {
-            q = s < n_mine ? c + ((i0 + s) % n_mine) * G : -1;
+            return idx < T ? ready_tile(p, static_cast<int>(idx)) : -1;
         }
+        return s < n_mine ? c + ((i0 + s) % n_mine) * G : -1;
+    };
 
+    LoaderRing rg;
+    uint32_t tq = 0, tqphase = 0;
+    bool ok = true;
+    bool serial_pending = (p.sync_mode == OPW_SYNC_SERIAL);
+    int q = tile_at(0);
+    int pre_kt = 0;  // flag columns of tile q acquired while the previous tile loaded
+
+    for (int s = 0; ok; ++s) {
         // Hand the tile to the MMA and epilogue warps (-1 = no more work).
         if (!wait_bar(&ctrl->tq_empty[tq], tqphase ^ 1u, ec, SITE_TILE_QUEUE)) break;
         if (lane == 0) {
@@ -189,95 +300,52 @@ __device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
         if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
         if (q < 0) break;
 
+        const int q_next = tile_at(s + 1);  // one tile of lookahead
         const int m0 = (q / p.T_N) * BM;
         const int n0 = (q % p.T_N) * BN;
         if (p.trace != nullptr && lane == 0) {
             const int F = p.R * p.T_mr * p.T_k;
             p.trace[2 * F + q] = (static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(s);
+            p.trace[2 * F + T + q] = globaltimer();
         }
         if (serial_pending) {
             if (!wait_all_published(p, ec)) break;
             serial_pending = false;
         }
+        int base0, base1;
+        flag_rows(p, m0, base0, base1);
+        int nb0 = -1, nb1 = -1;
+        if (q_next >= 0) flag_rows(p, (q_next / p.T_N) * BM, nb0, nb1);
 
-        // Flag rows covered by rows [m0, m0 + BM): one (flag tile 128) or two (64).
-        int base0, base1 = -1;
-        {
-            const int r = m0 / p.M_r;
-            const int mt = (m0 - r * p.M_r) / p.ft;
-            base0 = (r * p.T_mr + mt) * p.T_k;
-            if (p.ft < BM && m0 + p.ft < p.M) {
-                const int g = m0 + p.ft;
-                const int r1 = g / p.M_r;
-                const int mt1 = (g - r1 * p.M_r) / p.ft;
-                base1 = (r1 * p.T_mr + mt1) * p.T_k;
+        // Acquire flags, then load only k-blocks whose flags are acquired.
+        // Just before the last STAGES k-blocks, look once (without waiting)
+        // at the next tile's flags, so the next tile boundary needs no round trip.
+        int ready_kt = pre_kt;
+        pre_kt = 0;
+        bool looked_ahead = (q_next < 0);
+        int kb = 0;
+        while (kb < KB && ok) {
+            if (kb >= ready_kt * kb_per_col) {
+                if (!acquire_flags(p, ec, base0, base1, ready_kt)) { ok = false; break; }
+                consume_token();
             }
+            const int kb_ready = min(KB, ready_kt * kb_per_col);
+            if (!looked_ahead && kb_ready == KB) {
+                const int split = max(kb, KB - STAGES);
+                if (!issue_kblocks(p, smem, ctrl, ec, rg, m0, n0, kb, split)) { ok = false; break; }
+                kb = split;
+                pre_kt = peek_flags(p, nb0, nb1);
+                if (pre_kt > 0) consume_token();
+                looked_ahead = true;
+            }
+            if (!issue_kblocks(p, smem, ctrl, ec, rg, m0, n0, kb, kb_ready)) { ok = false; break; }
+            kb = kb_ready;
         }
-
-        int ready_kt = 0;
-        bool fresh = false;  // flags acquired since the last TMA issue
-        uint64_t wait_t0 = 0;
-        for (int kb = 0; kb < KB && ok; ++kb) {
-            const int kt = (kb * BK) / p.ft;
-            // Acquire: no load of this A tile before its flag shows the epoch.
-            uint32_t spins = 0;
-            while (kt >= ready_kt) {
-                const int n = poll_flags(p, base0, base1, ready_kt);
-                if (n > 0) {
-                    ready_kt += n;
-                    fresh = true;
-                    spins = 0;
-                    continue;
-                }
-                if (spins == 0) wait_t0 = globaltimer();
-                ++spins;
-                __nanosleep(128);
-                if ((spins & 7u) == 0) {
-                    if (aborted(ec)) { ok = false; break; }
-                    if (globaltimer() - wait_t0 > ec.timeout_ns) {
-                        if (lane == 0) {
-                            // report the first missing slot
-                            const int slot = base0 + ready_kt;
-                            const int rank = slot / (p.T_mr * p.T_k);
-                            raise_error(ec, OPW_ERR_TIMEOUT, rank, slot);
-                        }
-                        ok = false;
-                        break;
-                    }
-                }
-            }
-            if (!ok) break;
-            __syncwarp();
-            if (!wait_bar(&ctrl->empty[stage], sphase ^ 1u, ec, SITE_LOADER_EMPTY)) { ok = false; break; }
-            if (lane == 0) {
-                // consume_token: order the flag acquires (made by every lane of
-                // this warp) before the async-proxy reads of the tile.
-                if (fresh) {
-                    fence_acq_rel_gpu();
-                    fence_async_global();
-                }
-                if (kb == 0 && p.trace != nullptr) {
-                    const int F = p.R * p.T_mr * p.T_k;
-                    p.trace[2 * F + T + q] = globaltimer();
-                }
-                uint64_t* fb = &ctrl->full[stage];
-                mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
-                tma_load_2d(smem + OFF_A + stage * A_STAGE_BYTES, &p.g_load, fb, kb * BK, m0);
-                uint8_t* bs = smem + OFF_B + stage * B_STAGE_BYTES;
-#pragma unroll
-                for (int j = 0; j < BN / 64; ++j)
-                    tma_load_2d(bs + j * B_CHUNK_BYTES, &p.b_load, fb, n0 + 64 * j, kb * BK);
-            }
-            __syncwarp();
-            fresh = false;
-            filled |= 1u << stage;
-            last_par = (last_par & ~(1u << stage)) | (sphase << stage);
-            if (++stage == STAGES) { stage = 0; sphase ^= 1u; }
-        }
+        q = q_next;
     }
     // Every TMA load this warp issued must land before the CTA may exit.
     for (int st = 0; st < STAGES; ++st)
-        if (filled & (1u << st)) drain_bar(&ctrl->full[st], (last_par >> st) & 1u, ec);
+        if (rg.filled & (1u << st)) drain_bar(&ctrl->full[st], (rg.last_par >> st) & 1u, ec);
 }
 
 // ------------------------------------------------------------------ MMA

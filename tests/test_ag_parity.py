@@ -132,7 +132,7 @@ def test_serial_mode_matches_overlap_bit_for_bit(api):
 
 def test_ready_schedule_matches_swizzle_bit_for_bit(api):
     d = inputs.ag_inputs(_cfg(4, 256, 512, 768), seed=11)
-    p1 = _run_and_check(api, d)
+    p1 = _run_and_check(api, d, opts_fn=lambda i: api.make_opts(schedule=api.SCHED_SWIZZLE))
     p2 = _run_and_check(api, d, epoch_runs=3,
                         opts_fn=lambda i: api.make_opts(schedule=api.SCHED_READY))
     assert np.array_equal(host_bits(p1.C), host_bits(p2.C))
@@ -177,7 +177,8 @@ def test_trace_publish_before_consume_and_swizzle_order(api):
     words = api.ag_trace_words(R, M_r, N, K)
     trace = torch.full((words,), -1, dtype=torch.int64, device="cuda")
     grid = 6
-    prob.run(api, sig, sig.next_epoch(), api.make_opts(trace=trace, num_ctas=grid))
+    prob.run(api, sig, sig.next_epoch(), api.make_opts(trace=trace, num_ctas=grid,
+                                                       schedule=api.SCHED_SWIZZLE))
     assert sig.status()[0] == api.OK
     v = _trace_views(api, prob, trace, grid)
     # every tile published, and no consumer acquired a tile before its publish
