@@ -300,7 +300,6 @@ __device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
         if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
         if (q < 0) break;
 
-        const int q_next = tile_at(s + 1);  // one tile of lookahead
         const int m0 = (q / p.T_N) * BM;
         const int n0 = (q % p.T_N) * BN;
         if (p.trace != nullptr && lane == 0) {
@@ -314,15 +313,15 @@ __device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
         }
         int base0, base1;
         flag_rows(p, m0, base0, base1);
-        int nb0 = -1, nb1 = -1;
-        if (q_next >= 0) flag_rows(p, (q_next / p.T_N) * BM, nb0, nb1);
 
         // Acquire flags, then load only k-blocks whose flags are acquired.
-        // Just before the last STAGES k-blocks, look once (without waiting)
-        // at the next tile's flags, so the next tile boundary needs no round trip.
+        // Just before the last STAGES k-blocks, take the next tile (a claim
+        // on the dynamic schedule) and look once, without waiting, at its
+        // flags, so the next tile boundary needs no round trip.
         int ready_kt = pre_kt;
         pre_kt = 0;
-        bool looked_ahead = (q_next < 0);
+        int q_next = -1;
+        bool looked_ahead = false;
         int kb = 0;
         while (kb < KB && ok) {
             if (kb >= ready_kt * kb_per_col) {
@@ -334,8 +333,13 @@ __device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
                 const int split = max(kb, KB - STAGES);
                 if (!issue_kblocks(p, smem, ctrl, ec, rg, m0, n0, kb, split)) { ok = false; break; }
                 kb = split;
-                pre_kt = peek_flags(p, nb0, nb1);
-                if (pre_kt > 0) consume_token();
+                q_next = tile_at(s + 1);
+                if (q_next >= 0) {
+                    int nb0, nb1;
+                    flag_rows(p, (q_next / p.T_N) * BM, nb0, nb1);
+                    pre_kt = peek_flags(p, nb0, nb1);
+                    if (pre_kt > 0) consume_token();
+                }
                 looked_ahead = true;
             }
             if (!issue_kblocks(p, smem, ctrl, ec, rg, m0, n0, kb, kb_ready)) { ok = false; break; }
