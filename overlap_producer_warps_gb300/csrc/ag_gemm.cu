@@ -77,12 +77,21 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, const 
     }
 }
 
-// Tile visited at position `idx` of the dynamic schedule: output rows in the
-// order their flag tiles are published, all column tiles of a row together.
+// Tile visited at position `idx` of the dynamic schedule.  Output row tiles
+// are taken in the order their flag tiles are published, in groups of
+// p.group_rows rows; within a group the column index runs slowest, so when B
+// is larger than L2 can hold next to everything else, the CTAs working at
+// the same time share B column tiles instead of streaming all of B for
+// every few rows (group_rows = 1 when B fits).
 __device__ __forceinline__ int ready_tile(const AgParams& p, int idx)
 {
-    const int mp = idx / p.T_N;
-    const int n = idx - mp * p.T_N;
+    const int GM = p.group_rows;
+    const int group = idx / (GM * p.T_N);
+    const int first = group * GM;
+    const int rows = min(GM, p.T_M - first);
+    const int local = idx - first * p.T_N;
+    const int mp = first + local % rows;
+    const int n = local / rows;
     int m = mp;
     if (p.ft == BM && p.M_r % BM == 0) {
         const int tpr = p.M_r / BM;

@@ -195,6 +195,8 @@ extern "C" opw_status opw_ag_gemm_noalloc(const opw_symm* symm, size_t a_off, in
     p.role = OPW_ROLE_FUSED;
     p.sync_mode = o.sync_mode;
     p.schedule = o.schedule;
+    // Row groups only pay when B (K x N bf16) is too big to stay in L2.
+    p.group_rows = (K * N * 2 > (int64_t(64) << 20)) ? 16 : 1;
     p.has_perm = o.publish_perm != nullptr;
     p.has_delay = o.delay_ns != nullptr;
     p.fault_kind = o.fault_kind;
