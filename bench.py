@@ -327,6 +327,16 @@ def per_config_results(api, torch, peak_tflops, reps=5):
 
         t_fused = time_launches(torch, fused, reps)
         t_swz = time_launches(torch, lambda: fused(schedule=api.SCHED_SWIZZLE), reps)
+        sig_add = api.Signal(api.ag_num_row_counters(R, M_r, K))
+
+        def fused_row_add():
+            api.ag_gemm(heap, d["rank_off"], d["a_off"], M_r, N, K, B, G, C, sig_add,
+                        sig_add.next_epoch(), api.make_opts(signal_mode=api.SIGNAL_ROW_ADD, **skew))
+
+        t_add = time_launches(torch, fused_row_add, reps)
+        if sig_add.status()[0] != api.OK:
+            raise RuntimeError(f"{name}: device error with row-ADD signals")
+        sig_add.close()
         t_prod = time_launches(torch, producer_only, reps)
         t_cons = time_launches(torch, consumer_only, reps)
         st = sig.status()
@@ -347,9 +357,10 @@ def per_config_results(api, torch, peak_tflops, reps=5):
         out[name] = {
             "fused_tflops": fl / t_fused / 1e9, "pct_of_peak": fl / t_fused / 1e9 / peak_tflops,
             "swizzle_schedule_tflops": fl / t_swz / 1e9,
+            "row_add_signal_tflops": fl / t_add / 1e9,
             "unfused_copy_then_gemm_tflops": fl / t_unf / 1e9,
             "cublas_gemm_only_tflops": fl / t_gemm / 1e9,
-            "ms": {"fused": t_fused, "swizzle": t_swz, "producer_only": t_prod,
+            "ms": {"fused": t_fused, "swizzle": t_swz, "row_add": t_add, "producer_only": t_prod,
                    "consumer_only": t_cons, "unfused": t_unf, "gemm_only": t_gemm},
             "overlap_efficiency": max(0.0, min(1.0, e)),
             "gather_hbm_gbs_producer_only": 2.0 * M * K * 2 / (t_prod * 1e-3) / 1e9,

@@ -151,6 +151,17 @@ typedef struct {
 #define OPW_ROLE_CONSUMER 2  /* only wait + GEMM; the epoch must already be
                                 published by an earlier producer launch */
 
+#define OPW_SIGNAL_TILE_SET 0  /* one flag per flag tile, SET to the epoch (default) */
+#define OPW_SIGNAL_ROW_ADD  1  /* one counter per flag row (rank r, row tile mt):
+                                  the producer ADDs 1 per published k-tile
+                                  (SignalOp ADD, "Distributed Architecture Design"
+                                  2.3); a consumer starts on the row only when the
+                                  counter reaches epoch * K/ft, i.e. every k-tile of
+                                  the row is in ("Batch Signals When Possible",
+                                  Best Practices 4).  Counters are cumulative, so a
+                                  signal object must keep one mode and one K/ft
+                                  between resets. */
+
 #define OPW_FAULT_NONE        0
 #define OPW_FAULT_DROP_TILE   1  /* the producer never publishes flag slot fault_arg */
 #define OPW_FAULT_STALE_EPOCH 2  /* the producer publishes epoch-1 into slot fault_arg */
@@ -170,6 +181,8 @@ typedef struct {
     uint64_t* trace_dev;          /* device [opw_ag_trace_words()] or NULL; see below */
     int32_t fault_kind;           /* OPW_FAULT_* (fault injection on the host-chosen slot) */
     int32_t fault_arg;
+    int32_t signal_mode;          /* OPW_SIGNAL_* (AG-GEMM only) */
+    int32_t reserved;             /* must be 0 */
 } opw_opts;
 
 /* Fill *o with the defaults (all fields 0 / NULL). */
@@ -185,6 +198,10 @@ void opw_opts_default(opw_opts* o);
  */
 int64_t opw_ag_flag_tile(int64_t M_r, int64_t K);
 int64_t opw_ag_num_flags(int32_t R, int64_t M_r, int64_t K);
+
+/* Counters needed with OPW_SIGNAL_ROW_ADD: R * (M_r/ft); counter of flag row
+ * (r, mt) is slot r * (M_r/ft) + mt.  -1 for invalid sizes. */
+int64_t opw_ag_num_row_counters(int32_t R, int64_t M_r, int64_t K);
 
 /*
  * Trace layout (uint64 words), written only when opts.trace_dev != NULL:
@@ -211,7 +228,8 @@ int64_t opw_ag_trace_words(int32_t R, int64_t M_r, int64_t N, int64_t K);
  *   B_dev   : [K, N] bf16.
  *   G_dev   : [R*M_r, K] bf16 gathered buffer, written by the producer warps.
  *   C_dev   : [R*M_r, N] bf16 output.
- *   sig     : at least opw_ag_num_flags(R, M_r, K) slots.
+ *   sig     : at least opw_ag_num_flags(R, M_r, K) slots
+ *             (opw_ag_num_row_counters with OPW_SIGNAL_ROW_ADD).
  *   epoch   : opw_signal_next_epoch() for FUSED / PRODUCER roles; for the
  *             CONSUMER role, the epoch an earlier PRODUCER launch published.
  *   opts    : NULL = defaults.

@@ -12,7 +12,7 @@ function cites the passage of the pages it follows:
 
 * "Triton-distributed Semantics" -- sections "AllGather and GEMM Overlapping",
   "GEMM and ReduceScatter Overlapping", "Threadblock Swizzling".
-* "Distributed Architecture Design" -- section 2.3 (SignalOp SET) and
+* "Distributed Architecture Design" -- section 2.3 (SignalOp SET and ADD) and
   section 5.3 (remote address resolution of symm_at).
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
@@ -90,6 +90,8 @@ def _load():
                                                    ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                                    ctypes.c_int64, ctypes.c_int64, _i64p, _f32p]),
             "opw_oracle_expected_flags": (None, [ctypes.c_int64, ctypes.c_int64, _i64p]),
+            "opw_oracle_expected_row_counters": (None, [ctypes.c_int64, ctypes.c_int64,
+                                                        ctypes.c_int64, _i64p]),
             "opw_oracle_swizzle_row": (ctypes.c_int64, [ctypes.c_int64] * 4),
             "opw_oracle_consumer_order": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64,
                                                            ctypes.c_int, ctypes.c_int64,
@@ -223,6 +225,12 @@ def gemm_rs_rows_f32(heap, rank_off, R, a_off, b_off, M, N, K_r, rows) -> np.nda
 def expected_flags(n_slots: int, epoch: int) -> np.ndarray:
     out = np.empty(n_slots, dtype=np.int64)
     _load().opw_oracle_expected_flags(n_slots, epoch, _p(out, _i64p))
+    return out
+
+
+def expected_row_counters(n_rows: int, epoch: int, T_k: int) -> np.ndarray:
+    out = np.empty(n_rows, dtype=np.int64)
+    _load().opw_oracle_expected_row_counters(n_rows, epoch, T_k, _p(out, _i64p))
     return out
 
 

@@ -335,6 +335,20 @@ void opw_oracle_expected_flags(int64_t n_slots, int64_t epoch, int64_t* out)
     for (int64_t i = 0; i < n_slots; ++i) out[i] = epoch;
 }
 
+/*
+ * Batched signals with SignalOp ADD ("Distributed Architecture Design", 2.3:
+ * ADD adds the given value to the current signal value; "Triton-distributed
+ * Semantics", Best Practices 4: tiles that are always consumed together may
+ * share one signal).  One counter per row of flag tiles; every launch adds 1
+ * for each of the row's T_k k-tiles, starting from 0 after a reset.  After
+ * the launches with epochs 1..e every counter holds e * T_k, which is also the
+ * value a consumer waits for to know the whole row is in.
+ */
+void opw_oracle_expected_row_counters(int64_t n_rows, int64_t epoch, int64_t T_k, int64_t* out)
+{
+    for (int64_t i = 0; i < n_rows; ++i) out[i] = epoch * T_k;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Consumer schedule (threadblock swizzle)                                   */
 /* ------------------------------------------------------------------------ */

@@ -30,6 +30,7 @@ SYNC_OVERLAP, SYNC_SERIAL = 0, 1
 SCHED_READY, SCHED_SWIZZLE = 0, 1
 ROLE_FUSED, ROLE_PRODUCER, ROLE_CONSUMER = 0, 1, 2
 FAULT_NONE, FAULT_DROP_TILE, FAULT_STALE_EPOCH = 0, 1, 2
+SIGNAL_TILE_SET, SIGNAL_ROW_ADD = 0, 1
 MAX_RANKS = 8
 TRACE_MAX_CTAS = 1024
 
@@ -49,7 +50,8 @@ class Opts(ctypes.Structure):
                 ("publish_perm", ctypes.POINTER(ctypes.c_int32)),
                 ("delay_ns", ctypes.POINTER(ctypes.c_uint32)),
                 ("trace_dev", ctypes.c_void_p), ("fault_kind", ctypes.c_int32),
-                ("fault_arg", ctypes.c_int32)]
+                ("fault_arg", ctypes.c_int32), ("signal_mode", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 _vp = ctypes.c_void_p
@@ -66,6 +68,8 @@ SIGNATURES = {
     "opw_opts_default": (None, [ctypes.POINTER(Opts)]),
     "opw_ag_flag_tile": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64]),
     "opw_ag_num_flags": (ctypes.c_int64, [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64]),
+    "opw_ag_num_row_counters": (ctypes.c_int64, [ctypes.c_int32, ctypes.c_int64,
+                                                 ctypes.c_int64]),
     "opw_ag_trace_words": (ctypes.c_int64, [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
                                             ctypes.c_int64]),
     "opw_ag_gemm": (ctypes.c_int32, [ctypes.POINTER(Symm), ctypes.c_size_t, ctypes.c_int64,
@@ -182,7 +186,7 @@ class Signal:
 
 def make_opts(timeout_ns=0, sync_mode=SYNC_OVERLAP, schedule=SCHED_READY, role=ROLE_FUSED,
               num_ctas=0, publish_perm=None, delay_ns=None, trace=None, fault_kind=FAULT_NONE,
-              fault_arg=0):
+              fault_arg=0, signal_mode=SIGNAL_TILE_SET):
     """Build an Opts struct; array arguments are kept alive on the struct."""
     o = Opts()
     lib().opw_opts_default(ctypes.byref(o))
@@ -204,6 +208,7 @@ def make_opts(timeout_ns=0, sync_mode=SYNC_OVERLAP, schedule=SCHED_READY, role=R
         o.trace_dev = trace.data_ptr()
     o.fault_kind = int(fault_kind)
     o.fault_arg = int(fault_arg)
+    o.signal_mode = int(signal_mode)
     o._keep = keep
     return o
 
@@ -225,6 +230,10 @@ def ag_flag_tile(M_r: int, K: int) -> int:
 
 def ag_num_flags(R: int, M_r: int, K: int) -> int:
     return int(lib().opw_ag_num_flags(R, M_r, K))
+
+
+def ag_num_row_counters(R: int, M_r: int, K: int) -> int:
+    return int(lib().opw_ag_num_row_counters(R, M_r, K))
 
 
 def ag_trace_words(R: int, M_r: int, N: int, K: int) -> int:

@@ -156,6 +156,24 @@ __device__ __forceinline__ int poll_flags(const AgParams& p, int base0, int base
     return n;
 }
 
+// Batched signals: every column of the tile's flag row(s) is published once
+// the row counter reaches epoch * T_k.  Returns the columns newly ready
+// (all remaining ones, or 0).
+__device__ __forceinline__ int poll_rows(const AgParams& p, int base0, int base1, int ready_kt)
+{
+    const int64_t target = static_cast<int64_t>(p.epoch) * p.T_k;
+    bool ready = ld_acquire(p.flags + base0 / p.T_k) >= target;
+    if (base1 >= 0) ready = ready && (ld_acquire(p.flags + base1 / p.T_k) >= target);
+    ready = __all_sync(0xffffffffu, ready);
+    return ready ? p.T_k - ready_kt : 0;
+}
+
+__device__ __forceinline__ int poll_any(const AgParams& p, int base0, int base1, int ready_kt)
+{
+    return p.signal_mode == OPW_SIGNAL_ROW_ADD ? poll_rows(p, base0, base1, ready_kt)
+                                               : poll_flags(p, base0, base1, ready_kt);
+}
+
 // Acquire at least one more flag column of the tile (bounded wait): on
 // return ready_kt has advanced past every column already published.
 __device__ __noinline__ bool acquire_flags(const AgParams& p, const ErrCtx& ec, int base0,
@@ -164,12 +182,12 @@ __device__ __noinline__ bool acquire_flags(const AgParams& p, const ErrCtx& ec, 
     const uint32_t lane = lane_id();
     uint64_t t0 = 0;
     for (uint32_t spins = 0;; ++spins) {
-        const int n = poll_flags(p, base0, base1, ready_kt);
+        const int n = poll_any(p, base0, base1, ready_kt);
         if (n > 0) {
             ready_kt += n;
             // take any further columns that are already published, without waiting
             while (ready_kt < p.T_k) {
-                const int more = poll_flags(p, base0, base1, ready_kt);
+                const int more = poll_any(p, base0, base1, ready_kt);
                 if (more == 0) break;
                 ready_kt += more;
             }
@@ -181,8 +199,13 @@ __device__ __noinline__ bool acquire_flags(const AgParams& p, const ErrCtx& ec, 
             if (aborted(ec)) return false;
             if (globaltimer() - t0 > ec.timeout_ns) {
                 if (lane == 0) {
-                    const int slot = base0 + ready_kt;  // first missing slot
-                    raise_error(ec, OPW_ERR_TIMEOUT, slot / (p.T_mr * p.T_k), slot);
+                    if (p.signal_mode == OPW_SIGNAL_ROW_ADD) {
+                        const int row = base0 / p.T_k;  // the row counter waited on
+                        raise_error(ec, OPW_ERR_TIMEOUT, row / p.T_mr, row);
+                    } else {
+                        const int slot = base0 + ready_kt;  // first missing slot
+                        raise_error(ec, OPW_ERR_TIMEOUT, slot / (p.T_mr * p.T_k), slot);
+                    }
                 }
                 return false;
             }
@@ -195,7 +218,7 @@ __device__ __noinline__ int peek_flags(const AgParams& p, int base0, int base1)
 {
     int ready_kt = 0;
     while (ready_kt < p.T_k) {
-        const int n = poll_flags(p, base0, base1, ready_kt);
+        const int n = poll_any(p, base0, base1, ready_kt);
         if (n == 0) break;
         ready_kt += n;
     }
@@ -593,7 +616,14 @@ __device__ void run_gather(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
             // the publish time is read before the release, so no consumer can
             // observe the flag earlier than the recorded time
             const uint64_t t_pub = p.trace != nullptr ? globaltimer() : 0;
-            if (!skip) st_release(p.flags + slot, v);
+            if (p.signal_mode == OPW_SIGNAL_ROW_ADD) {
+                // batched signal: one counter per flag row, +1 per k-tile
+                if (!skip && v == static_cast<int64_t>(p.epoch))
+                    red_release_add(reinterpret_cast<unsigned long long*>(p.flags) + r * p.T_mr + mt,
+                                    1ull);
+            } else if (!skip) {
+                st_release(p.flags + slot, v);
+            }
             red_release_add(p.counters + CTR_RANK_DONE + r, 1ull);
             if (p.trace != nullptr) p.trace[slot] = t_pub;
         }

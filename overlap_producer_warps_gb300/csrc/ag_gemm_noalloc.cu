@@ -124,6 +124,9 @@ extern "C" opw_status opw_ag_gemm_noalloc(const opw_symm* symm, size_t a_off, in
     if (o.schedule != OPW_SCHED_SWIZZLE && o.schedule != OPW_SCHED_READY) return OPW_ERR_INVALID_ARG;
     if (o.fault_kind < OPW_FAULT_NONE || o.fault_kind > OPW_FAULT_STALE_EPOCH) return OPW_ERR_INVALID_ARG;
     if (o.num_ctas < 0) return OPW_ERR_INVALID_ARG;
+    if ((o.signal_mode != OPW_SIGNAL_TILE_SET && o.signal_mode != OPW_SIGNAL_ROW_ADD) ||
+        o.reserved != 0)
+        return OPW_ERR_INVALID_ARG;
     const int R = symm->R;
     if (o.publish_perm != nullptr) {
         bool seen[OPW_MAX_RANKS] = {};
@@ -197,6 +200,7 @@ extern "C" opw_status opw_ag_gemm_noalloc(const opw_symm* symm, size_t a_off, in
     p.schedule = o.schedule;
     // Row groups only pay when B (K x N bf16) is too big to stay in L2.
     p.group_rows = (K * N * 2 > (int64_t(64) << 20)) ? 16 : 1;
+    p.signal_mode = o.signal_mode;
     p.has_perm = o.publish_perm != nullptr;
     p.has_delay = o.delay_ns != nullptr;
     p.fault_kind = o.fault_kind;

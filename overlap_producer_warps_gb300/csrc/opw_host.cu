@@ -30,6 +30,8 @@ struct opw_signal {
     uint64_t rank_target_last[OPW_MAX_RANKS];  // targets of the last producing launch
     uint64_t claim_next;           // claim counter value after all enqueued launches
     bool latched;                  // opw_status_sync saw a device error
+    int32_t mode;                  // signal mode since the last reset (-1: none yet)
+    int64_t mode_tk;               // K/ft used with OPW_SIGNAL_ROW_ADD since the last reset
 };
 
 namespace {
@@ -59,6 +61,8 @@ opw_status reset_device(opw_signal* s, cudaStream_t st)
     for (int r = 0; r < OPW_MAX_RANKS; ++r) s->rank_done[r] = s->rank_target_last[r] = 0;
     s->claim_next = 0;
     s->latched = false;
+    s->mode = -1;
+    s->mode_tk = 0;
     return OPW_OK;
 }
 
@@ -258,6 +262,13 @@ int64_t opw_ag_num_flags(int32_t R, int64_t M_r, int64_t K)
     return static_cast<int64_t>(R) * (M_r / ft) * (K / ft);
 }
 
+int64_t opw_ag_num_row_counters(int32_t R, int64_t M_r, int64_t K)
+{
+    const int64_t ft = opw_ag_flag_tile(M_r, K);
+    if (ft < 0 || R < 1 || R > OPW_MAX_RANKS) return -1;
+    return static_cast<int64_t>(R) * (M_r / ft);
+}
+
 int64_t opw_ag_trace_words(int32_t R, int64_t M_r, int64_t N, int64_t K)
 {
     const int64_t F = opw_ag_num_flags(R, M_r, K);
@@ -282,6 +293,9 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
     if (o.role < OPW_ROLE_FUSED || o.role > OPW_ROLE_CONSUMER) return OPW_ERR_INVALID_ARG;
     if (o.fault_kind < OPW_FAULT_NONE || o.fault_kind > OPW_FAULT_STALE_EPOCH) return OPW_ERR_INVALID_ARG;
     if (o.num_ctas < 0) return OPW_ERR_INVALID_ARG;
+    if (o.signal_mode != OPW_SIGNAL_TILE_SET && o.signal_mode != OPW_SIGNAL_ROW_ADD)
+        return OPW_ERR_INVALID_ARG;
+    if (o.reserved != 0) return OPW_ERR_INVALID_ARG;
     const int R = symm->R;
     if (o.publish_perm != nullptr) {
         bool seen[OPW_MAX_RANKS] = {};
@@ -300,8 +314,12 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
         !aligned16(static_cast<int64_t>(a_off)) ||
         (o.trace_dev != nullptr && (reinterpret_cast<uintptr_t>(o.trace_dev) & 7u) != 0))
         return OPW_ERR_MISALIGNED;
-    const int64_t F = static_cast<int64_t>(R) * (M_r / ft) * (K / ft);
+    const bool row_add = o.signal_mode == OPW_SIGNAL_ROW_ADD;
+    const int64_t F = static_cast<int64_t>(R) * (M_r / ft) * (row_add ? 1 : K / ft);
     if (sig->num_slots < F) return OPW_ERR_INVALID_ARG;
+    // Row counters are cumulative: one mode (and one K/ft) until the next reset.
+    if (sig->mode >= 0 && (sig->mode != o.signal_mode || (row_add && sig->mode_tk != K / ft)))
+        return OPW_ERR_INVALID_ARG;
     if (sig->latched) return OPW_ERR_NOT_READY;
     const bool produces = o.role != OPW_ROLE_CONSUMER;
     if (produces ? epoch != sig->epoch_last + 1 : (epoch != sig->epoch_last || epoch == 0))
@@ -349,6 +367,7 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
     p.schedule = o.schedule;
     // Row groups only pay when B (K x N bf16) is too big to stay in L2.
     p.group_rows = (K * N * 2 > (int64_t(64) << 20)) ? 16 : 1;
+    p.signal_mode = o.signal_mode;
     p.has_perm = o.publish_perm != nullptr;
     p.has_delay = o.delay_ns != nullptr;
     p.fault_kind = o.fault_kind;
@@ -365,6 +384,8 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
         return OPW_ERR_CUDA;
 
     // ---- host bookkeeping for the next launch on this object
+    sig->mode = o.signal_mode;
+    sig->mode_tk = K / ft;
     if (produces) {
         sig->epoch_last = epoch;
         for (int r = 0; r < R; ++r) {
@@ -393,7 +414,8 @@ opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t 
     opw_opts tmp;
     const opw_opts& o = opts_or_default(opts_in, tmp);
     if (o.sync_mode != 0 || o.schedule != 0 || o.role != 0 || o.publish_perm != nullptr ||
-        o.delay_ns != nullptr || o.fault_kind != 0 || o.num_ctas < 0)
+        o.delay_ns != nullptr || o.fault_kind != 0 || o.num_ctas < 0 || o.signal_mode != 0 ||
+        o.reserved != 0)
         return OPW_ERR_INVALID_ARG;
     const int R = symm->R;
     if (M <= 0 || N <= 0 || K_r <= 0 || M % (128 * R) != 0 || N % 8 != 0 || K_r % 8 != 0)

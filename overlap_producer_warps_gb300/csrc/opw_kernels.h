@@ -64,6 +64,7 @@ struct AgParams {
     int32_t T_M, T_N;         // output tiles
     int32_t role, sync_mode, schedule;
     int32_t group_rows;       // dynamic schedule: row tiles per rasterisation group
+    int32_t signal_mode;      // OPW_SIGNAL_TILE_SET or OPW_SIGNAL_ROW_ADD
     int32_t has_perm, has_delay;
     int32_t fault_kind, fault_arg;
     int32_t perm[OPW_MAX_RANKS];

@@ -51,11 +51,11 @@ def test_struct_layout_matches_c_compiler(api):
 #include <stdio.h>
 #include "opw.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(opw_opts),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(opw_opts),
     offsetof(opw_opts, timeout_ns), offsetof(opw_opts, sync_mode), offsetof(opw_opts, schedule),
     offsetof(opw_opts, role), offsetof(opw_opts, num_ctas), offsetof(opw_opts, publish_perm),
     offsetof(opw_opts, delay_ns), offsetof(opw_opts, trace_dev), offsetof(opw_opts, fault_kind),
-    offsetof(opw_opts, fault_arg));
+    offsetof(opw_opts, fault_arg), offsetof(opw_opts, signal_mode), offsetof(opw_opts, reserved));
   printf("%zu %zu %zu %zu %zu\n", sizeof(opw_symm), offsetof(opw_symm, heap_dev),
     offsetof(opw_symm, rank_off), offsetof(opw_symm, R), offsetof(opw_symm, reserved));
   return 0;
@@ -91,6 +91,8 @@ def test_flag_geometry(api):
     assert api.ag_num_flags(8, 1024, 4096) == 2048      # 8 ranks x 8 x 32
     assert api.ag_num_flags(8, 4096, 8192) == 16384
     assert api.ag_num_flags(9, 128, 128) == -1
+    assert api.ag_num_row_counters(8, 1024, 4096) == 64   # 8 ranks x 8 row tiles
+    assert api.ag_num_row_counters(2, 64, 128) == 2
     assert api.rs_num_flags(8, 8192, 4096) == 2048      # 8 ranks x 8 x 32
     assert api.rs_num_flags(8, 8192 + 128, 4096) == -1
     F, T = 2048, 64 * 16
@@ -146,6 +148,7 @@ def test_ag_gemm_rejects_bad_arguments_on_the_host(api):
     assert _ag(api, opts=api.make_opts(role=3)) == E.ERR_INVALID_ARG
     assert _ag(api, opts=api.make_opts(publish_perm=[0, 0])) == E.ERR_INVALID_ARG
     assert _ag(api, opts=api.make_opts(publish_perm=[0, 2])) == E.ERR_INVALID_ARG
+    assert _ag(api, opts=api.make_opts(signal_mode=2)) == E.ERR_INVALID_ARG
     # a signal object with too few slots (here: none)
     assert _ag(api) == E.ERR_INVALID_ARG
 

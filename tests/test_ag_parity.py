@@ -246,3 +246,37 @@ def test_full_size_configs_sampled(api, name):
     rows = sample_rows(prob.M, 128 if per_tile else 512, per_tile, seed=1)
     C = host_bits(prob.C)
     assert_gemm_close(C[rows], prob.oracle_rows(rows), what=f"{name} sampled C")
+
+
+@pytest.mark.parametrize("R,M_r,K,N", [(4, 256, 512, 776), (2, 64, 128, 128), (3, 64, 192, 200)])
+def test_row_add_batched_signals(api, R, M_r, K, N):
+    """One ADD counter per flag row: counters == epoch * K/ft after each launch."""
+    d = inputs.ag_inputs(_cfg(R, M_r, K, N), seed=60 + R)
+    prob = AgProblem(d)
+    ft = api.ag_flag_tile(M_r, K)
+    n_rows = api.ag_num_row_counters(R, M_r, K)
+    sig = api.Signal(n_rows)
+    for _ in range(5):
+        e = sig.next_epoch()
+        prob.run(api, sig, e, api.make_opts(signal_mode=api.SIGNAL_ROW_ADD))
+        assert sig.status()[0] == api.OK
+        assert np.array_equal(sig.flags().cpu().numpy(),
+                              oracle.expected_row_counters(n_rows, e, K // ft))
+    G_ref, C_ref = prob.oracle_full()
+    assert np.array_equal(host_bits(prob.G), G_ref)
+    assert_gemm_close(host_bits(prob.C), C_ref)
+
+
+def test_row_add_and_tile_set_do_not_mix_without_reset(api):
+    d = inputs.ag_inputs(_cfg(2, 128, 256, 256), seed=70)
+    prob = AgProblem(d)
+    sig = api.Signal(api.ag_num_flags(2, 128, 256))
+    args = (prob.heap, prob.rank_off, prob.a_off, prob.M_r, prob.N, prob.K, prob.B, prob.G, prob.C)
+    assert api.ag_gemm_status(*args, sig, 1) == api.OK
+    add = api.make_opts(signal_mode=api.SIGNAL_ROW_ADD)
+    assert api.ag_gemm_status(*args, sig, 2, add) == api.ERR_INVALID_ARG
+    sig.reset()
+    assert api.ag_gemm_status(*args, sig, 1, add) == api.OK
+    assert sig.status()[0] == api.OK
+    _, C_ref = prob.oracle_full()
+    assert_gemm_close(host_bits(prob.C), C_ref)

@@ -76,3 +76,15 @@ def test_too_few_slots_and_misalignment(api):
     sig = api.Signal(api.ag_num_flags(4, 128, 256))
     assert api.ag_gemm_status(prob.heap, prob.rank_off, 8, prob.M_r, prob.N, prob.K, prob.B,
                               prob.G, prob.C, sig, 1) == api.ERR_MISALIGNED
+
+
+def test_row_add_missing_increment_times_out(api):
+    prob = _problem()
+    n_rows = api.ag_num_row_counters(4, 128, 256)
+    sig = api.Signal(n_rows)
+    # tile slot 5 = rank 2, row tile 0, k-tile 1: its row counter (slot 2) never completes
+    prob.run(api, sig, sig.next_epoch(), api.make_opts(timeout_ns=TIMEOUT_NS,
+                                                       fault_kind=api.FAULT_DROP_TILE, fault_arg=5,
+                                                       signal_mode=api.SIGNAL_ROW_ADD))
+    status, rank, where = sig.status()
+    assert (status, rank, where) == (api.ERR_TIMEOUT, 2, 2)

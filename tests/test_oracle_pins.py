@@ -269,6 +269,17 @@ def test_expected_flags_set_semantics():
     assert f.dtype == np.int64 and np.all(f == 13)
 
 
+def test_row_counters_against_simulated_adds():
+    # Brute force: replay every launch's per-k-tile ADD of 1 on zeroed counters.
+    for n_rows, T_k, epochs in [(1, 1, 1), (3, 4, 2), (8, 32, 5), (2, 2, 20)]:
+        counters = [0] * n_rows
+        for e in range(1, epochs + 1):
+            for row in range(n_rows):
+                for _ in range(T_k):
+                    counters[row] += 1
+            assert list(oracle.expected_row_counters(n_rows, e, T_k)) == counters
+
+
 def test_swizzle_golden(golden):
     fx = golden("swizzle.json")
     pf = fx["page_formula"]
