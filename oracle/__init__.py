@@ -11,7 +11,8 @@ only compiles it with gcc and marshals numpy arrays through ctypes.  Each
 function cites the passage of the pages it follows:
 
 * "Triton-distributed Semantics" -- sections "AllGather and GEMM Overlapping",
-  "GEMM and ReduceScatter Overlapping", "Threadblock Swizzling".
+  "GEMM and ReduceScatter Overlapping", "Threadblock Swizzling", "Example: Ring
+  AllReduce with Overlap".
 * "Distributed Architecture Design" -- section 2.3 (SignalOp SET and ADD) and
   section 5.3 (remote address resolution of symm_at).
 
@@ -92,6 +93,8 @@ def _load():
             "opw_oracle_expected_flags": (None, [ctypes.c_int64, ctypes.c_int64, _i64p]),
             "opw_oracle_expected_row_counters": (None, [ctypes.c_int64, ctypes.c_int64,
                                                         ctypes.c_int64, _i64p]),
+            "opw_oracle_ring_allreduce": (None, [_u8p, _i64p, ctypes.c_int, ctypes.c_int64,
+                                                 ctypes.c_int64, ctypes.c_int64, _u8p]),
             "opw_oracle_swizzle_row": (ctypes.c_int64, [ctypes.c_int64] * 4),
             "opw_oracle_consumer_order": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64,
                                                            ctypes.c_int, ctypes.c_int64,
@@ -244,3 +247,14 @@ def consumer_order(T_M: int, T_N: int, R: int, G: int, c: int) -> np.ndarray:
     out = np.empty(max(1, (T + G - 1) // G), dtype=np.int64)
     n = _load().opw_oracle_consumer_order(T_M, T_N, R, G, c, _p(out, _i64p))
     return out[:n].copy()
+
+
+# -- ring AllReduce -------------------------------------------------------------
+
+def ring_allreduce(heap, rank_off, R, data_off, out_off, n):
+    """heap_out (uint8, laid out like the heap) with every rank's fp32 result."""
+    heap, ro = _heap_args(heap, rank_off)
+    heap_out = heap.copy()
+    _load().opw_oracle_ring_allreduce(_p(heap, _u8p), _p(ro, _i64p), R, data_off, out_off, n,
+                                      _p(heap_out, _u8p))
+    return heap_out

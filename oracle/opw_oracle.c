@@ -387,3 +387,47 @@ int64_t opw_oracle_consumer_order(int64_t T_M, int64_t T_N, int R, int64_t G, in
     }
     return count;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Ring AllReduce                                                            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * "Triton-distributed Semantics", "Example: Ring AllReduce with Overlap".
+ * R ranks each hold n fp32 values at symmetric offset data_off, viewed as R
+ * chunks of n/R values.  Reduce-scatter: in R-1 steps each rank adds its own
+ * copy of a chunk to the partial sum it receives from the previous rank
+ * (reduced = local + incoming) and passes it on; the partial for chunk c
+ * starts at rank c, so its sum is taken in ring order c, c+1, ..., c-1:
+ *     S_c = x_{c-1}[c] + ( ... + (x_{c+2}[c] + (x_{c+1}[c] + x_c[c])) ... )
+ * in binary32 (indices mod R).  All-gather: R-1 more steps copy each finished
+ * chunk around the ring, so every rank ends with every S_c.  The result
+ * written at each rank's out_off is therefore concat_c(S_c) on every rank.
+ *
+ * Writes rank j's result at heap_out + rank_off[j] + out_off.
+ */
+void opw_oracle_ring_allreduce(const uint8_t* heap, const int64_t* rank_off, int R,
+                               int64_t data_off, int64_t out_off, int64_t n, uint8_t* heap_out)
+{
+    const int64_t chunk = n / R;
+    float* S = (float*)malloc((size_t)n * sizeof(float));
+    if (!S) return;
+    for (int c = 0; c < R; ++c) {
+        const float* x_c = (const float*)rank_ptr(heap, rank_off, c, data_off);
+        for (int64_t i = 0; i < chunk; ++i) S[c * chunk + i] = x_c[c * chunk + i];
+        for (int k = 1; k < R; ++k) {
+            const int r = (c + k) % R;
+            const float* x_r = (const float*)rank_ptr(heap, rank_off, r, data_off);
+            for (int64_t i = 0; i < chunk; ++i) {
+                const float local = x_r[c * chunk + i];
+                const float incoming = S[c * chunk + i];
+                S[c * chunk + i] = local + incoming;
+            }
+        }
+    }
+    for (int j = 0; j < R; ++j) {
+        float* out_j = (float*)(uintptr_t)rank_ptr(heap_out, rank_off, j, out_off);
+        memcpy(out_j, S, (size_t)n * sizeof(float));
+    }
+    free(S);
+}

@@ -312,3 +312,52 @@ def test_consumer_order_is_a_partition_starting_at_home_rank(T_M, T_N, R, G):
         keys = [(((q // T_N) - h * per) % T_M, q % T_N) for q in order]
         assert keys == sorted(keys)
     assert sorted(seen) == list(range(T_M * T_N))
+
+
+# ---------------------------------------------------------------- ring AllReduce
+
+def _ring_heap(xs, pad=64):
+    R, n = len(xs), len(xs[0])
+    sl = ((2 * n * 4 + pad - 1) // pad) * pad
+    heap = np.zeros(R * sl, dtype=np.uint8)
+    rank_off = np.array([((r + 1) % R) * sl for r in range(R)], dtype=np.int64)  # permuted table
+    for r in range(R):
+        heap[rank_off[r]:rank_off[r] + n * 4] = np.asarray(xs[r], dtype=np.float32).view(np.uint8)
+    return heap, rank_off, n * 4   # data at 0, out at n*4
+
+
+def _ring_out(heap_out, rank_off, R, out_off, n):
+    return [heap_out[rank_off[j] + out_off:rank_off[j] + out_off + n * 4].view(np.float32) for j in range(R)]
+
+
+def test_ring_allreduce_worked_examples(golden):
+    ex = golden("worked_examples.json")["ring_allreduce"]
+    for case in (ex, ex["fp32_order_case"]):
+        xs = case["x"]
+        R, n = len(xs), len(xs[0])
+        heap, ro, out_off = _ring_heap(xs)
+        outs = _ring_out(oracle.ring_allreduce(heap, ro, R, 0, out_off, n), ro, R, out_off, n)
+        for o in outs:
+            assert np.array_equal(o, np.array(case["sum"], dtype=np.float32))
+
+
+def test_ring_allreduce_exact_on_integers_and_identical_on_every_rank():
+    rng = np.random.default_rng(3)
+    for R in (1, 2, 3, 8):
+        n = R * 12
+        xs = [rng.integers(-1000, 1000, n).astype(np.float32) for _ in range(R)]
+        heap, ro, out_off = _ring_heap(xs)
+        outs = _ring_out(oracle.ring_allreduce(heap, ro, R, 0, out_off, n), ro, R, out_off, n)
+        exact = np.sum(np.stack(xs).astype(np.int64), axis=0)
+        for o in outs:
+            assert np.array_equal(o.astype(np.int64), exact)
+
+
+def test_ring_allreduce_within_binary32_bound():
+    rng = np.random.default_rng(4)
+    R, n = 8, 8 * 256
+    xs = [rng.standard_normal(n).astype(np.float32) for _ in range(R)]
+    heap, ro, out_off = _ring_heap(xs)
+    out = _ring_out(oracle.ring_allreduce(heap, ro, R, 0, out_off, n), ro, R, out_off, n)[0]
+    X = np.stack(xs).astype(np.float64)
+    assert np.all(np.abs(out - X.sum(0)) <= R * 2.0 ** -24 * np.abs(X).sum(0))
