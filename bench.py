@@ -289,6 +289,35 @@ def time_launches(torch, fn, n, warm=2):
     return e0.elapsed_time(e1) / n
 
 
+def ring_results(api, torch, reps, R=8, n=8 * (1 << 21)):
+    """Ring AllReduce over 8 logical ranks of n fp32 values (64 MiB per rank):
+    the HBM bytes its schedule moves per second, against the measured HBM peak."""
+    from overlap_producer_warps_gb300 import inputs
+    peaks, _ = load_peaks()
+    d = inputs.ring_inputs(R, n, seed=0)
+    heap = torch.from_numpy(d["heap"]).cuda()
+    sig = api.Signal(api.ring_num_flags(R, n))
+
+    def run():
+        api.ring_allreduce(heap, d["rank_off"], d["data_off"], d["recv_off"], d["out_off"], n, sig,
+                           sig.next_epoch())
+
+    t = time_launches(torch, run, reps)
+    st = sig.status()
+    if st[0] != api.OK:
+        raise RuntimeError(f"ring_allreduce: device error {st}")
+    chunk_b = (n // R) * 4
+    # per rank: send own chunk (r+w), R-2 forwarding reduce steps (2r+w), the last
+    # reduce step (2r+2w), R-2 forwarding gather steps (r+2w), the last gather step (r+w)
+    algo_bytes = R * chunk_b * (2 + 3 * (R - 2) + 4 + 3 * (R - 2) + 2)
+    gbs = algo_bytes / (t * 1e-3) / 1e9
+    busbw = 2 * (R - 1) / R * n * 4 / (t * 1e-3) / 1e9
+    sig.close()
+    return {"ranks": R, "values_per_rank": n, "ms": t, "hbm_gbs": gbs,
+            "hbm_frac": gbs / float(peaks["hbm_gbs"]), "algo_bytes": algo_bytes,
+            "busbw_gbs": busbw}
+
+
 def per_config_results(api, torch, peak_tflops, reps=5):
     """Each of the pages' tensor-parallel configurations on its own: fused
     TFLOP/s, the unfused copy-then-GEMM baseline, cuBLAS on the pre-gathered
@@ -368,6 +397,8 @@ def per_config_results(api, torch, peak_tflops, reps=5):
         sig.close()
         del heap, B, G, C, shards
         torch.cuda.empty_cache()
+
+    out["ring_allreduce"] = ring_results(api, torch, reps)
 
     cfg = inputs.CONFIGS["rs_tp"]
     d = inputs.rs_inputs(cfg, seed=0)

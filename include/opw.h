@@ -320,6 +320,38 @@ opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t 
                        int64_t M, int64_t N, int64_t K_r, opw_signal* sig, uint64_t epoch,
                        const opw_opts* opts, void* stream);
 
+/* ---------------------------------------------------------- ring AllReduce */
+
+/*
+ * Tile-centric ring AllReduce over the R logical ranks ("Triton-distributed
+ * Semantics", "Example: Ring AllReduce with Overlap").  Rank r holds n fp32
+ * values at heap_dev + rank_off[r] + data_off, viewed as R chunks of n/R.
+ * Reduce-scatter: chunk c's partial starts at rank c and visits ranks c+1,
+ * c+2, ... (mod R), each adding its own copy (reduced = local + incoming,
+ * binary32, round to nearest); all-gather: the finished chunks go around the
+ * ring once more.  On return every rank's out_off holds the same n values.
+ *
+ * Each chunk is cut into pieces of 1024 values that move independently; the
+ * piece arriving at rank r in ring step g sits in r's receive area at
+ * recv_off + 4*(g*n/R + piece offset) and is announced by flag slot
+ * (r*(2R-2) + g)*P + piece, P = ceil((n/R)/1024), set to the epoch with a
+ * .gpu release; the receiver acquires it (>= epoch) before reading.
+ *
+ *   data_off : n fp32 per rank (input, not modified)
+ *   recv_off : opw_ring_recv_bytes(R, n) bytes per rank (scratch owned by the
+ *              caller; contents are overwritten)
+ *   out_off  : n fp32 per rank (output); must not overlap data or recv
+ *   sig      : at least opw_ring_num_flags(R, n) slots; epoch = next epoch
+ *   opts     : NULL or defaults except timeout_ns / num_ctas
+ * Shapes: n a multiple of 4*R.  Offsets and rank_off[] multiples of 16.
+ * Errors as for opw_ag_gemm.
+ */
+int64_t opw_ring_num_flags(int32_t R, int64_t n);
+int64_t opw_ring_recv_bytes(int32_t R, int64_t n);
+opw_status opw_ring_allreduce(const opw_symm* symm, size_t data_off, size_t recv_off,
+                              size_t out_off, int64_t n, opw_signal* sig, uint64_t epoch,
+                              const opw_opts* opts, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

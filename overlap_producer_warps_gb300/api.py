@@ -79,6 +79,11 @@ SIGNATURES = {
                                              ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _vp,
                                              _vp, _vp, _vp, ctypes.POINTER(Opts), _vp]),
     "opw_rs_num_flags": (ctypes.c_int64, [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64]),
+    "opw_ring_num_flags": (ctypes.c_int64, [ctypes.c_int32, ctypes.c_int64]),
+    "opw_ring_recv_bytes": (ctypes.c_int64, [ctypes.c_int32, ctypes.c_int64]),
+    "opw_ring_allreduce": (ctypes.c_int32, [ctypes.POINTER(Symm), ctypes.c_size_t,
+                                            ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int64,
+                                            _vp, ctypes.c_uint64, ctypes.POINTER(Opts), _vp]),
     "opw_gemm_rs": (ctypes.c_int32, [ctypes.POINTER(Symm), ctypes.c_size_t, ctypes.c_size_t,
                                      ctypes.c_size_t, ctypes.c_int64, ctypes.c_int64,
                                      ctypes.c_int64, _vp, ctypes.c_uint64, ctypes.POINTER(Opts),
@@ -295,3 +300,27 @@ def gemm_rs(heap, rank_off, a_off, b_off, out_off, M, N, K_r, sig: Signal, epoch
     """GEMM -> ReduceScatter (see opw_gemm_rs).  Asynchronous on `stream`."""
     _check(gemm_rs_status(heap, rank_off, a_off, b_off, out_off, M, N, K_r, sig, epoch, opts,
                           stream), "opw_gemm_rs")
+
+
+def ring_num_flags(R: int, n: int) -> int:
+    return int(lib().opw_ring_num_flags(R, n))
+
+
+def ring_recv_bytes(R: int, n: int) -> int:
+    return int(lib().opw_ring_recv_bytes(R, n))
+
+
+def ring_allreduce_status(heap, rank_off, data_off, recv_off, out_off, n, sig: Signal, epoch,
+                          opts=None, stream=None) -> int:
+    s = _symm(heap, rank_off)
+    return int(lib().opw_ring_allreduce(ctypes.byref(s), int(data_off), int(recv_off),
+                                        int(out_off), int(n), sig.handle, int(epoch),
+                                        ctypes.byref(opts) if opts is not None else None,
+                                        _stream_ptr(stream)))
+
+
+def ring_allreduce(heap, rank_off, data_off, recv_off, out_off, n, sig: Signal, epoch,
+                   opts=None, stream=None):
+    """Tile-centric ring AllReduce over the logical ranks (see opw_ring_allreduce)."""
+    _check(ring_allreduce_status(heap, rank_off, data_off, recv_off, out_off, n, sig, epoch,
+                                 opts, stream), "opw_ring_allreduce")

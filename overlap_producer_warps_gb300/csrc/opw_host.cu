@@ -16,24 +16,6 @@
 
 using namespace opw;
 
-// ---------------------------------------------------------------- signal object
-
-struct opw_signal {
-    int device;
-    int64_t num_slots;
-    void* mem;                     // one device allocation: flags | status | counters
-    int64_t* flags;                // [num_slots]
-    int32_t* status;               // [4]: code, rank, slot, reserved
-    unsigned long long* counters;  // [CTR_WORDS]
-    uint64_t epoch_last;           // last epoch published (host view)
-    uint64_t rank_done[OPW_MAX_RANKS];       // expected rank counters after all enqueued launches
-    uint64_t rank_target_last[OPW_MAX_RANKS];  // targets of the last producing launch
-    uint64_t claim_next;           // claim counter value after all enqueued launches
-    bool latched;                  // opw_status_sync saw a device error
-    int32_t mode;                  // signal mode since the last reset (-1: none yet)
-    int64_t mode_tk;               // K/ft used with OPW_SIGNAL_ROW_ADD since the last reset
-};
-
 namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;

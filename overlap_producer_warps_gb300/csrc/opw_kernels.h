@@ -87,6 +87,20 @@ struct RsParams {
     int32_t T_fm, T_fn;       // 128x128 flag tiles per rank block along M, along N
 };
 
+struct RingParams {
+    char* heap;
+    int64_t rank_off[OPW_MAX_RANKS];
+    int64_t data_off, recv_off, out_off;  // byte offsets inside every rank's slice
+    int64_t chunk;                        // fp32 values per chunk (n / R)
+    int32_t R, P;                         // ranks, pieces per chunk
+    int64_t* flags;
+    int32_t* status;
+    uint64_t epoch;
+    uint64_t timeout_ns;
+};
+
+constexpr int RING_PIECE = 1024;  // fp32 values one warp moves per ring action
+
 // Shared memory each kernel asks for (dynamic, includes 1 KiB alignment slack).
 size_t ag_smem_bytes();
 size_t rs_smem_bytes();
@@ -94,5 +108,26 @@ size_t rs_smem_bytes();
 // Launch helpers (cooperative launch so every CTA is co-resident).
 cudaError_t launch_ag_gemm(const AgParams& p, int grid, cudaStream_t s);
 cudaError_t launch_gemm_rs(const RsParams& p, int grid, cudaStream_t s);
+cudaError_t launch_ring_allreduce(const RingParams& p, int sms, cudaStream_t s);
 
 }  // namespace opw
+
+// Signal object behind the opaque opw_signal handle (host side).
+
+struct opw_signal {
+    int device;
+    int64_t num_slots;
+    void* mem;                     // one device allocation: flags | status | counters
+    int64_t* flags;                // [num_slots]
+    int32_t* status;               // [4]: code, rank, slot, reserved
+    unsigned long long* counters;  // [CTR_WORDS]
+    uint64_t epoch_last;           // last epoch published (host view)
+    uint64_t rank_done[OPW_MAX_RANKS];       // expected rank counters after all enqueued launches
+    uint64_t rank_target_last[OPW_MAX_RANKS];  // targets of the last producing launch
+    uint64_t claim_next;           // claim counter value after all enqueued launches
+    bool latched;                  // opw_status_sync saw a device error
+    int32_t mode;                  // signal mode since the last reset (-1: none yet)
+    int64_t mode_tk;               // K/ft used with OPW_SIGNAL_ROW_ADD since the last reset
+};
+
+

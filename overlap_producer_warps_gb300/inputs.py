@@ -133,3 +133,25 @@ def skew_schedule(seed: int, R: int):
     perm = rng.permutation(R).astype(np.int32)
     delay_us = rng.integers(0, 51, size=R)
     return perm, (delay_us * 1000).astype(np.uint32)
+
+
+def ring_layout(R: int, n: int):
+    """Heap layout for the ring AllReduce: data, receive area, output."""
+    data_off = 0
+    recv_off = _align(n * 4)
+    out_off = recv_off + _align(max(1, 2 * R - 2) * (n // R) * 4)
+    slice_bytes = out_off + _align(n * 4)
+    return dict(data_off=data_off, recv_off=recv_off, out_off=out_off, slice_bytes=slice_bytes)
+
+
+def ring_inputs(R: int, n: int, seed: int = 0, slot_order=None, scale: float = 1.0):
+    """fp32 normal(0, scale) data per rank (tensor id A), placed in the heap."""
+    lay = ring_layout(R, n)
+    rank_off = rank_offsets(R, lay["slice_bytes"], slot_order)
+    heap = np.zeros(R * lay["slice_bytes"], dtype=np.uint8)
+    for r in range(R):
+        rng = np.random.default_rng([seed, TENSOR_A, r])
+        x = rng.standard_normal(n, dtype=np.float32) * np.float32(scale)
+        o = int(rank_off[r]) + lay["data_off"]
+        heap[o:o + n * 4] = x.view(np.uint8)
+    return dict(heap=heap, rank_off=rank_off, R=R, n=n, **lay)

@@ -95,6 +95,10 @@ def test_flag_geometry(api):
     assert api.ag_num_row_counters(2, 64, 128) == 2
     assert api.rs_num_flags(8, 8192, 4096) == 2048      # 8 ranks x 8 x 32
     assert api.rs_num_flags(8, 8192 + 128, 4096) == -1
+    assert api.ring_num_flags(8, 8 * 4096) == 8 * 14 * 4      # 4 pieces of 1024 per chunk
+    assert api.ring_num_flags(3, 3 * 400) == 3 * 4 * 1
+    assert api.ring_num_flags(3, 1001) == -1
+    assert api.ring_recv_bytes(8, 8 * 4096) == 14 * 4096 * 4
     F, T = 2048, 64 * 16
     assert api.ag_trace_words(8, 1024, 4096, 4096) == 2 * F + 2 * T + api.TRACE_MAX_CTAS
 
@@ -177,3 +181,19 @@ def test_signal_alloc_without_gpu_reports_cuda_error(api):
     assert h.value is None
     assert api.lib().opw_signal_alloc(None, 16, None) == api.ERR_INVALID_ARG
     assert api.lib().opw_signal_free(None) == api.OK
+
+
+def test_ring_allreduce_rejects_bad_arguments_on_the_host(api):
+    s = _fake_sig()
+
+    def ring(n=4096, R=4, data_off=0, recv_off=65536, out_off=262144, opts=None):
+        return api.ring_allreduce_status(_Fake(0x100000), [i * (1 << 20) for i in range(R)],
+                                         data_off, recv_off, out_off, n, s, 1, opts,
+                                         stream=_NoStream())
+
+    assert ring(n=4098) == api.ERR_UNSUPPORTED_SHAPE     # not a multiple of 4R
+    assert ring(n=0) == api.ERR_UNSUPPORTED_SHAPE
+    assert ring(recv_off=8) == api.ERR_MISALIGNED
+    assert ring(opts=api.make_opts(sync_mode=1)) == api.ERR_INVALID_ARG
+    assert ring(R=9) == api.ERR_INVALID_ARG
+    assert ring() == api.ERR_INVALID_ARG                   # too few slots
