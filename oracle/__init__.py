@@ -13,6 +13,7 @@ function cites the passage of the pages it follows:
 * "Triton-distributed Semantics" -- sections "AllGather and GEMM Overlapping",
   "GEMM and ReduceScatter Overlapping", "Threadblock Swizzling", "Example: Ring
   AllReduce with Overlap".
+* Aboleth README -- Tier-2 all-to-all (put, signal with epoch, wait).
 * "Distributed Architecture Design" -- section 2.3 (SignalOp SET and ADD) and
   section 5.3 (remote address resolution of symm_at).
 
@@ -95,6 +96,8 @@ def _load():
                                                         ctypes.c_int64, _i64p]),
             "opw_oracle_ring_allreduce": (None, [_u8p, _i64p, ctypes.c_int, ctypes.c_int64,
                                                  ctypes.c_int64, ctypes.c_int64, _u8p]),
+            "opw_oracle_alltoall": (None, [_u8p, _i64p, ctypes.c_int, ctypes.c_int64,
+                                           ctypes.c_int64, ctypes.c_int64, _u8p]),
             "opw_oracle_swizzle_row": (ctypes.c_int64, [ctypes.c_int64] * 4),
             "opw_oracle_consumer_order": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64,
                                                            ctypes.c_int, ctypes.c_int64,
@@ -257,4 +260,15 @@ def ring_allreduce(heap, rank_off, R, data_off, out_off, n):
     heap_out = heap.copy()
     _load().opw_oracle_ring_allreduce(_p(heap, _u8p), _p(ro, _i64p), R, data_off, out_off, n,
                                       _p(heap_out, _u8p))
+    return heap_out
+
+
+# -- all-to-all -----------------------------------------------------------------
+
+def alltoall(heap, rank_off, R, send_off, recv_off, B):
+    """heap_out with every rank's receive buffer filled (B bytes per slice)."""
+    heap, ro = _heap_args(heap, rank_off)
+    heap_out = heap.copy()
+    _load().opw_oracle_alltoall(_p(heap, _u8p), _p(ro, _i64p), R, send_off, recv_off, B,
+                                _p(heap_out, _u8p))
     return heap_out

@@ -431,3 +431,28 @@ void opw_oracle_ring_allreduce(const uint8_t* heap, const int64_t* rank_off, int
     }
     free(S);
 }
+
+/* ------------------------------------------------------------------------ */
+/* All-to-all                                                                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Aboleth README, Tier-2 all-to-all: every rank puts slice `peer` of its send
+ * buffer into the peer's receive buffer at position RANK, then signals the
+ * peer.  The plain result: rank j's receive buffer holds, at slot r, slice j
+ * of rank r's send buffer:
+ *     recv_j[r*B .. (r+1)*B) = send_r[j*B .. (j+1)*B)    for all ranks r, j
+ * (B bytes per slice; the slot r == j is the rank's own slice, copied too).
+ * Written into heap_out, laid out like the heap.
+ */
+void opw_oracle_alltoall(const uint8_t* heap, const int64_t* rank_off, int R, int64_t send_off,
+                         int64_t recv_off, int64_t B, uint8_t* heap_out)
+{
+    for (int j = 0; j < R; ++j) {
+        uint8_t* recv_j = (uint8_t*)(uintptr_t)rank_ptr(heap_out, rank_off, j, recv_off);
+        for (int r = 0; r < R; ++r) {
+            const uint8_t* send_r = rank_ptr(heap, rank_off, r, send_off);
+            memcpy(recv_j + (int64_t)r * B, send_r + (int64_t)j * B, (size_t)B);
+        }
+    }
+}

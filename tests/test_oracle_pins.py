@@ -361,3 +361,41 @@ def test_ring_allreduce_within_binary32_bound():
     out = _ring_out(oracle.ring_allreduce(heap, ro, R, 0, out_off, n), ro, R, out_off, n)[0]
     X = np.stack(xs).astype(np.float64)
     assert np.all(np.abs(out - X.sum(0)) <= R * 2.0 ** -24 * np.abs(X).sum(0))
+
+
+# ---------------------------------------------------------------- all-to-all
+
+def _a2a_heap(sends, B, pad=64):
+    R = len(sends)
+    sl = ((2 * R * B + pad - 1) // pad) * pad
+    heap = np.zeros(R * sl, dtype=np.uint8)
+    rank_off = np.array([((r + 2) % R) * sl for r in range(R)], dtype=np.int64)  # permuted
+    for r in range(R):
+        heap[rank_off[r]:rank_off[r] + R * B] = np.asarray(sends[r], dtype=np.uint8).reshape(-1)
+    return heap, rank_off, R * B   # send at 0, recv at R*B
+
+
+def test_alltoall_worked_example(golden):
+    ex = golden("worked_examples.json")["alltoall"]
+    R, B = 3, 1
+    heap, ro, recv_off = _a2a_heap(ex["send"], B)
+    out = oracle.alltoall(heap, ro, R, 0, recv_off, B)
+    for j in range(R):
+        got = out[ro[j] + recv_off:ro[j] + recv_off + R * B]
+        assert list(got) == ex["recv"][j]
+
+
+def test_alltoall_is_an_involution_and_a_permutation_of_bytes():
+    rng = np.random.default_rng(8)
+    for R, B in [(1, 16), (2, 48), (5, 32), (8, 64)]:
+        sends = [rng.integers(0, 256, R * B, dtype=np.uint8) for _ in range(R)]
+        heap, ro, recv_off = _a2a_heap(sends, B)
+        once = oracle.alltoall(heap, ro, R, 0, recv_off, B)
+        recvs = [once[ro[j] + recv_off:ro[j] + recv_off + R * B].copy() for j in range(R)]
+        # every input byte appears exactly once
+        assert sorted(np.concatenate(recvs).tolist()) == sorted(np.concatenate(sends).tolist())
+        # applying it again to the receive buffers gives back the send buffers
+        heap2, ro2, recv_off2 = _a2a_heap(recvs, B)
+        twice = oracle.alltoall(heap2, ro2, R, 0, recv_off2, B)
+        for j in range(R):
+            assert np.array_equal(twice[ro2[j] + recv_off2:ro2[j] + recv_off2 + R * B], sends[j])
