@@ -318,6 +318,28 @@ def ring_results(api, torch, reps, R=8, n=8 * (1 << 21)):
             "busbw_gbs": busbw}
 
 
+def alltoall_results(api, torch, reps, R=8, B=8 << 20):
+    """All-to-all over 8 logical ranks, 8 MiB per (sender, receiver) slice."""
+    from overlap_producer_warps_gb300 import inputs
+    peaks, _ = load_peaks()
+    d = inputs.alltoall_inputs(R, B, seed=0)
+    heap = torch.from_numpy(d["heap"]).cuda()
+    sig = api.Signal(api.alltoall_num_flags(R, B))
+
+    def run():
+        api.alltoall(heap, d["rank_off"], d["send_off"], d["recv_off"], B, sig, sig.next_epoch())
+
+    t = time_launches(torch, run, reps)
+    st = sig.status()
+    if st[0] != api.OK:
+        raise RuntimeError(f"alltoall: device error {st}")
+    moved = 2 * R * R * B  # every slice read once and written once
+    gbs = moved / (t * 1e-3) / 1e9
+    sig.close()
+    return {"ranks": R, "bytes_per_slice": B, "ms": t, "hbm_gbs": gbs,
+            "hbm_frac": gbs / float(peaks["hbm_gbs"])}
+
+
 def per_config_results(api, torch, peak_tflops, reps=5):
     """Each of the pages' tensor-parallel configurations on its own: fused
     TFLOP/s, the unfused copy-then-GEMM baseline, cuBLAS on the pre-gathered
@@ -399,6 +421,7 @@ def per_config_results(api, torch, peak_tflops, reps=5):
         torch.cuda.empty_cache()
 
     out["ring_allreduce"] = ring_results(api, torch, reps)
+    out["alltoall"] = alltoall_results(api, torch, reps)
 
     cfg = inputs.CONFIGS["rs_tp"]
     d = inputs.rs_inputs(cfg, seed=0)

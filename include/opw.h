@@ -352,6 +352,29 @@ opw_status opw_ring_allreduce(const opw_symm* symm, size_t data_off, size_t recv
                               size_t out_off, int64_t n, opw_signal* sig, uint64_t epoch,
                               const opw_opts* opts, void* stream);
 
+/* -------------------------------------------------------------- all-to-all */
+
+/*
+ * All-to-all over the R logical ranks with put + signal + epoch (Aboleth
+ * README, Tier-2 all-to-all): rank r's send buffer holds R slices of
+ * bytes_per_peer bytes at heap_dev + rank_off[r] + send_off; afterwards
+ * rank j's receive buffer (recv_off, R slices) holds at slot r the slice j of
+ * rank r's send buffer.  Slices move in 4 KiB pieces; each piece sent to a
+ * peer is announced by flag slot (j*R + r)*P + piece = epoch (.gpu release),
+ * P = ceil(bytes_per_peer / 4096), and every receiver acquires all of its
+ * incoming flags (>= epoch) before the call completes.  The rank's own slice
+ * is copied without a flag.
+ *
+ *   sig  : at least opw_alltoall_num_flags(R, bytes_per_peer) slots; epoch =
+ *          next epoch.   opts: NULL or defaults except timeout_ns / num_ctas.
+ * Shapes: bytes_per_peer a multiple of 16.  Offsets and rank_off[] multiples
+ * of 16; send and receive buffers must not overlap.  Errors as opw_ag_gemm.
+ */
+int64_t opw_alltoall_num_flags(int32_t R, int64_t bytes_per_peer);
+opw_status opw_alltoall(const opw_symm* symm, size_t send_off, size_t recv_off,
+                        int64_t bytes_per_peer, opw_signal* sig, uint64_t epoch,
+                        const opw_opts* opts, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -79,6 +79,10 @@ SIGNATURES = {
                                              ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _vp,
                                              _vp, _vp, _vp, ctypes.POINTER(Opts), _vp]),
     "opw_rs_num_flags": (ctypes.c_int64, [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64]),
+    "opw_alltoall_num_flags": (ctypes.c_int64, [ctypes.c_int32, ctypes.c_int64]),
+    "opw_alltoall": (ctypes.c_int32, [ctypes.POINTER(Symm), ctypes.c_size_t, ctypes.c_size_t,
+                                      ctypes.c_int64, _vp, ctypes.c_uint64, ctypes.POINTER(Opts),
+                                      _vp]),
     "opw_ring_num_flags": (ctypes.c_int64, [ctypes.c_int32, ctypes.c_int64]),
     "opw_ring_recv_bytes": (ctypes.c_int64, [ctypes.c_int32, ctypes.c_int64]),
     "opw_ring_allreduce": (ctypes.c_int32, [ctypes.POINTER(Symm), ctypes.c_size_t,
@@ -324,3 +328,23 @@ def ring_allreduce(heap, rank_off, data_off, recv_off, out_off, n, sig: Signal, 
     """Tile-centric ring AllReduce over the logical ranks (see opw_ring_allreduce)."""
     _check(ring_allreduce_status(heap, rank_off, data_off, recv_off, out_off, n, sig, epoch,
                                  opts, stream), "opw_ring_allreduce")
+
+
+def alltoall_num_flags(R: int, bytes_per_peer: int) -> int:
+    return int(lib().opw_alltoall_num_flags(R, bytes_per_peer))
+
+
+def alltoall_status(heap, rank_off, send_off, recv_off, bytes_per_peer, sig: Signal, epoch,
+                    opts=None, stream=None) -> int:
+    s = _symm(heap, rank_off)
+    return int(lib().opw_alltoall(ctypes.byref(s), int(send_off), int(recv_off),
+                                  int(bytes_per_peer), sig.handle, int(epoch),
+                                  ctypes.byref(opts) if opts is not None else None,
+                                  _stream_ptr(stream)))
+
+
+def alltoall(heap, rank_off, send_off, recv_off, bytes_per_peer, sig: Signal, epoch, opts=None,
+             stream=None):
+    """All-to-all over the logical ranks with put + signal + epoch (see opw_alltoall)."""
+    _check(alltoall_status(heap, rank_off, send_off, recv_off, bytes_per_peer, sig, epoch, opts,
+                           stream), "opw_alltoall")

@@ -155,3 +155,19 @@ def ring_inputs(R: int, n: int, seed: int = 0, slot_order=None, scale: float = 1
         o = int(rank_off[r]) + lay["data_off"]
         heap[o:o + n * 4] = x.view(np.uint8)
     return dict(heap=heap, rank_off=rank_off, R=R, n=n, **lay)
+
+
+def alltoall_inputs(R: int, bytes_per_peer: int, seed: int = 0, slot_order=None):
+    """Random send buffers (uniform bytes, tensor id A) and an empty receive area."""
+    B = bytes_per_peer
+    send_off = 0
+    recv_off = _align(R * B)
+    slice_bytes = recv_off + _align(R * B)
+    rank_off = rank_offsets(R, slice_bytes, slot_order)
+    heap = np.zeros(R * slice_bytes, dtype=np.uint8)
+    for r in range(R):
+        rng = np.random.default_rng([seed, TENSOR_A, r])
+        o = int(rank_off[r]) + send_off
+        heap[o:o + R * B] = rng.integers(0, 256, R * B, dtype=np.uint8)
+    return dict(heap=heap, rank_off=rank_off, R=R, B=B, send_off=send_off, recv_off=recv_off,
+                slice_bytes=slice_bytes)

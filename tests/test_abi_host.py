@@ -99,6 +99,9 @@ def test_flag_geometry(api):
     assert api.ring_num_flags(3, 3 * 400) == 3 * 4 * 1
     assert api.ring_num_flags(3, 1001) == -1
     assert api.ring_recv_bytes(8, 8 * 4096) == 14 * 4096 * 4
+    assert api.alltoall_num_flags(8, 65536) == 8 * 8 * 16
+    assert api.alltoall_num_flags(3, 48) == 9
+    assert api.alltoall_num_flags(3, 40) == -1
     F, T = 2048, 64 * 16
     assert api.ag_trace_words(8, 1024, 4096, 4096) == 2 * F + 2 * T + api.TRACE_MAX_CTAS
 
@@ -197,3 +200,16 @@ def test_ring_allreduce_rejects_bad_arguments_on_the_host(api):
     assert ring(opts=api.make_opts(sync_mode=1)) == api.ERR_INVALID_ARG
     assert ring(R=9) == api.ERR_INVALID_ARG
     assert ring() == api.ERR_INVALID_ARG                   # too few slots
+
+
+def test_alltoall_rejects_bad_arguments_on_the_host(api):
+    s = _fake_sig()
+
+    def a2a(B=4096, R=4, send_off=0, recv_off=65536, opts=None):
+        return api.alltoall_status(_Fake(0x100000), [i * (1 << 20) for i in range(R)], send_off,
+                                   recv_off, B, s, 1, opts, stream=_NoStream())
+
+    assert a2a(B=40) == api.ERR_UNSUPPORTED_SHAPE
+    assert a2a(send_off=4) == api.ERR_MISALIGNED
+    assert a2a(opts=api.make_opts(role=1)) == api.ERR_INVALID_ARG
+    assert a2a() == api.ERR_INVALID_ARG                    # too few slots
