@@ -8,18 +8,19 @@
 // own rank's rows and rotate ("Threadblock Swizzling").
 //
 // One CTA per SM, 8 warps:
-//   warp 0     loader: acquires the flags of the A tiles a k-block needs, then
-//              TMA-loads the A tile from the gathered buffer G and the B tile
-//              into a 4-stage shared-memory ring.  Owns the tile schedule.
-//              Flag acquisition sits outside the k-block loop, and the next
-//              tile's flags are looked at while the current tile's last
-//              stages load, so the loop itself is a plain GEMM pipeline.
+//   warp 0     loader: takes tiles from the on-chip tile queue and TMA-loads
+//              their A k-blocks from the gathered buffer G and B k-blocks into
+//              a 4-stage shared-memory ring: a plain GEMM pipeline.
 //   warp 1     MMA: one thread issues tcgen05.mma (bf16 x bf16 -> fp32) into a
 //              double-buffered TMEM accumulator (2 x 128 lanes x 256 columns).
 //   warp 2     gather producer: TMA-copies flag tiles of A_r into G through
 //              shared memory, waits for the copy to complete, and publishes the
 //              tile's flag with st.release.gpu.
-//   warp 3     allocates / frees TMEM.
+//   warp 3     allocates / frees TMEM; in between it is the scheduler: it
+//              picks the next output tile, acquires (ld.acquire.gpu) the flags
+//              of all the A tiles that output tile needs, and only then puts
+//              it on the tile queue.  Acquiring ahead of the loader keeps every
+//              global-memory round trip off the k-block loop.
 //   warps 4-7  epilogue: tcgen05.ld -> bf16 (round to nearest even) ->
 //              swizzled shared memory -> TMA store of C.
 // Every wait is bounded: on timeout the kernel latches an error in the
@@ -39,6 +40,7 @@ struct AgCtrl {
     uint64_t gfull[2];
     uint64_t tq_full[TILE_Q];
     uint64_t tq_empty[TILE_Q];
+    uint64_t need_next;  // loader -> scheduler: claim the next tile now
     uint64_t mma_done;
     int32_t tile_q[TILE_Q];
     uint32_t tmem_base;
@@ -54,6 +56,13 @@ constexpr int SMEM_ALLOC = OFF_CTRL + static_cast<int>(sizeof(AgCtrl)) + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget (227 KiB per CTA)");
 static_assert(OFF_B % 1024 == 0 && OFF_EPI % 1024 == 0 && OFF_GATHER % 1024 == 0,
               "swizzled buffers must be 1024-byte aligned");
+
+// The loader asks for its next tile this many k-blocks before the end of the
+// current one: late enough that a CTA never holds more than one tile it has
+// not started (the dynamic schedule stays greedy, so CTAs that wait longer on
+// the gather do not end up with fewer tiles), early enough to hide the flag
+// acquire and the first TMA loads.
+constexpr int CLAIM_LEAD_KB = 64;
 
 constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators of 256 columns
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, /*B MN-major*/ true);
@@ -213,18 +222,6 @@ __device__ __noinline__ bool acquire_flags(const AgParams& p, const ErrCtx& ec, 
     }
 }
 
-// How many leading flag columns of a tile are already published (no wait).
-__device__ __noinline__ int peek_flags(const AgParams& p, int base0, int base1)
-{
-    int ready_kt = 0;
-    while (ready_kt < p.T_k) {
-        const int n = poll_any(p, base0, base1, ready_kt);
-        if (n == 0) break;
-        ready_kt += n;
-    }
-    return ready_kt;
-}
-
 // ------------------------------------------------------------------ loader
 
 // Flag rows covered by output rows [m0, m0 + BM): one for 128-row flag tiles,
@@ -273,25 +270,12 @@ __device__ __forceinline__ bool issue_kblocks(const AgParams& p, uint8_t* smem, 
     return true;
 }
 
-// consume_token: order the flag acquires (made by every lane of this warp)
-// before any later async-proxy read issued by lane 0.
-__device__ __forceinline__ void consume_token()
-{
-    if (lane_id() == 0) {
-        fence_acq_rel_gpu();
-        fence_async_global();
-    }
-    __syncwarp();
-}
-
-__device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const ErrCtx& ec)
+__device__ void run_scheduler(const AgParams& p, AgCtrl* ctrl, const ErrCtx& ec)
 {
     const uint32_t lane = lane_id();
     const int G = static_cast<int>(gridDim.x);
     const int c = static_cast<int>(blockIdx.x);
     const int T = p.T_M * p.T_N;
-    const int KB = p.K / BK;
-    const int kb_per_col = p.ft / BK;  // k-blocks per flag column
 
     // Static schedule: this CTA owns tiles q = c + i*G; it starts at the first
     // one in its home rank's rows (h*tiles_per_pe row tiles down) and wraps.
@@ -301,83 +285,85 @@ __device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
     int i0 = start_q <= c ? 0 : static_cast<int>((start_q - c + G - 1) / G);
     if (i0 >= n_mine) i0 = 0;
 
-    // Tile at visit position s (-1 = none).  The dynamic schedule claims from
-    // the device counter; tiles come out in the order their rows are published.
-    auto tile_at = [&](int s) -> int {
+    uint32_t tq = 0, tqphase = 0;
+    bool serial_pending = (p.sync_mode == OPW_SYNC_SERIAL);
+    for (int s = 0;; ++s) {
+        // Claim tile s only when the loader asks for it (it has reached the
+        // last CLAIM_LEAD_KB k-blocks of tile s-1; phases cannot alias, since
+        // the loader has popped at most s tiles) and a queue slot is free.
+        if (s > 0 && !wait_bar(&ctrl->need_next, (s - 1) & 1u, ec, SITE_TILE_QUEUE)) return;
+        if (!wait_bar(&ctrl->tq_empty[tq], tqphase ^ 1u, ec, SITE_TILE_QUEUE)) return;
+        int q;
         if (p.schedule == OPW_SCHED_READY) {
             long long idx = 0;
             if (lane == 0)
                 idx = static_cast<long long>(atomicAdd(p.counters + CTR_CLAIM, 1ull) - p.claim_base);
             idx = __shfl_sync(0xffffffffu, idx, 0);
-            return idx < T ? ready_tile(p, static_cast<int>(idx)) : -1;
+            q = idx < T ? ready_tile(p, static_cast<int>(idx)) : -1;
+        } else {
+            q = s < n_mine ? c + ((i0 + s) % n_mine) * G : -1;
         }
-        return s < n_mine ? c + ((i0 + s) % n_mine) * G : -1;
-    };
-
-    LoaderRing rg;
-    uint32_t tq = 0, tqphase = 0;
-    bool ok = true;
-    bool serial_pending = (p.sync_mode == OPW_SYNC_SERIAL);
-    int q = tile_at(0);
-    int pre_kt = 0;  // flag columns of tile q acquired while the previous tile loaded
-
-    for (int s = 0; ok; ++s) {
-        // Hand the tile to the MMA and epilogue warps (-1 = no more work).
-        if (!wait_bar(&ctrl->tq_empty[tq], tqphase ^ 1u, ec, SITE_TILE_QUEUE)) break;
+        if (q >= 0) {
+            if (p.trace != nullptr && lane == 0) {
+                const int F = p.R * p.T_mr * p.T_k;
+                p.trace[2 * F + q] = (static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(s);
+                p.trace[2 * F + T + q] = globaltimer();
+            }
+            if (serial_pending) {
+                if (!wait_all_published(p, ec)) return;
+                serial_pending = false;
+            }
+            // Acquire: no load of this tile's A rows before all their flags show the epoch.
+            int base0, base1;
+            flag_rows(p, (q / p.T_N) * BM, base0, base1);
+            int ready_kt = 0;
+            while (ready_kt < p.T_k)
+                if (!acquire_flags(p, ec, base0, base1, ready_kt)) return;
+            // every lane's acquire precedes lane 0's release through the queue
+            __syncwarp();
+            if (lane == 0) fence_acq_rel_gpu();
+            __syncwarp();
+        }
+        // Hand the tile over (-1 = no more work).
         if (lane == 0) {
             reinterpret_cast<volatile int32_t*>(ctrl->tile_q)[tq] = q;
-            mbar_arrive(&ctrl->tq_full[tq]);
+            mbar_arrive(&ctrl->tq_full[tq]);  // release: the acquires above come first
+        }
+        __syncwarp();
+        if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
+        if (q < 0) return;
+    }
+}
+
+// ------------------------------------------------------------------ loader
+
+// Warp 0: takes tiles from the queue (their flags already acquired) and
+// streams their k-blocks through the shared-memory ring.
+__device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const ErrCtx& ec)
+{
+    const uint32_t lane = lane_id();
+    const int KB = p.K / BK;
+    LoaderRing rg;
+    uint32_t tq = 0, tqphase = 0;
+    while (true) {
+        if (!wait_bar(&ctrl->tq_full[tq], tqphase, ec, SITE_TILE_QUEUE)) break;
+        const int q = reinterpret_cast<volatile int32_t*>(ctrl->tile_q)[tq];
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&ctrl->tq_empty[tq]);
+            // consume_token: the scheduler's flag acquires reach this thread
+            // through the queue barrier; order them before the async-proxy
+            // reads of the tile.
+            if (q >= 0) fence_async_global();
         }
         __syncwarp();
         if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
         if (q < 0) break;
-
-        const int m0 = (q / p.T_N) * BM;
-        const int n0 = (q % p.T_N) * BN;
-        if (p.trace != nullptr && lane == 0) {
-            const int F = p.R * p.T_mr * p.T_k;
-            p.trace[2 * F + q] = (static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(s);
-            p.trace[2 * F + T + q] = globaltimer();
-        }
-        if (serial_pending) {
-            if (!wait_all_published(p, ec)) break;
-            serial_pending = false;
-        }
-        int base0, base1;
-        flag_rows(p, m0, base0, base1);
-
-        // Acquire flags, then load only k-blocks whose flags are acquired.
-        // Just before the last STAGES k-blocks, take the next tile (a claim
-        // on the dynamic schedule) and look once, without waiting, at its
-        // flags, so the next tile boundary needs no round trip.
-        int ready_kt = pre_kt;
-        pre_kt = 0;
-        int q_next = -1;
-        bool looked_ahead = false;
-        int kb = 0;
-        while (kb < KB && ok) {
-            if (kb >= ready_kt * kb_per_col) {
-                if (!acquire_flags(p, ec, base0, base1, ready_kt)) { ok = false; break; }
-                consume_token();
-            }
-            const int kb_ready = min(KB, ready_kt * kb_per_col);
-            if (!looked_ahead && kb_ready == KB) {
-                const int split = max(kb, KB - STAGES);
-                if (!issue_kblocks(p, smem, ctrl, ec, rg, m0, n0, kb, split)) { ok = false; break; }
-                kb = split;
-                q_next = tile_at(s + 1);
-                if (q_next >= 0) {
-                    int nb0, nb1;
-                    flag_rows(p, (q_next / p.T_N) * BM, nb0, nb1);
-                    pre_kt = peek_flags(p, nb0, nb1);
-                    if (pre_kt > 0) consume_token();
-                }
-                looked_ahead = true;
-            }
-            if (!issue_kblocks(p, smem, ctrl, ec, rg, m0, n0, kb, kb_ready)) { ok = false; break; }
-            kb = kb_ready;
-        }
-        q = q_next;
+        const int m0 = (q / p.T_N) * BM, n0 = (q % p.T_N) * BN;
+        const int kb_ask = KB > CLAIM_LEAD_KB ? KB - CLAIM_LEAD_KB : 0;
+        if (!issue_kblocks(p, smem, ctrl, ec, rg, m0, n0, 0, kb_ask)) break;
+        if (lane == 0) mbar_arrive(&ctrl->need_next);
+        if (!issue_kblocks(p, smem, ctrl, ec, rg, m0, n0, kb_ask, KB)) break;
     }
     // Every TMA load this warp issued must land before the CTA may exit.
     for (int st = 0; st < STAGES; ++st)
@@ -656,8 +642,9 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
         }
         for (int i = 0; i < TILE_Q; ++i) {
             mbar_init(&ctrl->tq_full[i], 1);
-            mbar_init(&ctrl->tq_empty[i], 1 + 4);
+            mbar_init(&ctrl->tq_empty[i], 1 + 1 + 4);  // loader, MMA, 4 epilogue warps
         }
+        mbar_init(&ctrl->need_next, 1);
         mbar_init(&ctrl->mma_done, 1);
         // A device error latched by an earlier launch: do nothing.
         ctrl->abort = ld_relaxed_s32(p.status) != 0 ? 1 : 0;
@@ -694,6 +681,8 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
         if (consumer) run_mma(p, smem, ctrl, tmem, ec);
     } else if (warp == 2) {
         if (producer) run_gather(p, smem, ctrl, ec, t_start);
+    } else if (warp == 3) {
+        if (consumer) run_scheduler(p, ctrl, ec);
     } else if (warp >= 4) {
         if (consumer) run_epilogue(p, smem, ctrl, tmem, ec, warp);
     }

@@ -352,8 +352,11 @@ __device__ __forceinline__ bool aborted(const ErrCtx& e)
 }
 
 // Bounded mbarrier wait.  Returns false (after latching an error) if the
-// phase does not complete within the timeout or another part of the grid
-// has already failed.  `who` tags the waiting role in the status word.
+// phase does not complete in time or another part of the grid has already
+// failed.  `who` tags the waiting role in the status word.  On-chip barriers
+// only stall as a consequence of some other wait (a flag that never comes,
+// which has its own bound), so they get four times the timeout: the wait
+// that names the root cause always runs out first.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const ErrCtx& e,
                                          int32_t who)
 {
@@ -363,7 +366,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const E
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 15u) == 0) {
             if (aborted(e)) return false;
-            if (globaltimer() - t0 > e.timeout_ns) {
+            if (globaltimer() - t0 > 4 * e.timeout_ns) {
                 raise_error(e, OPW_ERR_TIMEOUT, -1, who);
                 return false;
             }
