@@ -8,16 +8,22 @@
 // on-chip mbarrier on a TMEM accumulator; the finished row block is written
 // into its logical rank's slice and published there with st.release.gpu.
 //
-// One CTA per SM, 12 warps:
-//   warp 0      loader: TMA-loads A_r / B_r k-blocks for rank r = 0..R-1 in
-//               order into a 4-stage shared-memory ring.
-//   warp 1      MMA: one thread issues tcgen05.mma; each rank's partial
-//               P_r = A_r * B_r goes into a fresh fp32 TMEM accumulator,
-//               alternating between two 256-column buffers.
-//   warp 2      allocates / frees TMEM.
+// CTAs work in pairs (clusters of 2) on 256 x 256 output tiles with one
+// tcgen05 cta_group::2 MMA: CTA c of the pair holds rows 128c..128c+127 of
+// A_r and columns 128c..128c+127 of B_r in its shared memory and receives rows
+// 128c.. of the accumulator in its own TMEM.  Against one CTA per 128 x 256
+// tile this moves a third less operand data from L2 per FLOP and leaves room
+// for a 6-stage ring.  12 warps per CTA:
+//   warp 0      loader (both CTAs): TMA-loads this CTA's half of every A_r / B_r
+//               k-block, for rank r = 0..R-1 in order; the bytes of both
+//               halves complete on the even CTA's `full` barrier.
+//   warp 1      MMA (even CTA only): one thread issues the pair's MMAs; each
+//               rank's partial P_r = A_r * B_r goes into a fresh fp32 TMEM
+//               accumulator, alternating between two 256-column buffers.
+//   warp 2      allocates / frees the pair's TMEM.
 //   warp 3      idle.
-//   warps 4-11  reduction: warp w reads TMEM lanes 32*(w&3).. and columns
-//               128*((w-4)>>2)..+127 of each partial and adds it into a
+//   warps 4-11  reduction (both CTAs): warp w reads TMEM lanes 32*(w&3).. and
+//               columns 128*((w-4)>>2)..+127 of each partial and adds it into a
 //               running fp32 sum held in registers, in rank order 0..R-1
 //               (S = ((0 + P_0) + P_1) + ...); then rounds S to bf16, stores
 //               the rows to rank j = row / (M/R) with TMA, and publishes the
@@ -30,26 +36,32 @@ namespace {
 
 constexpr int RS_THREADS = 384;
 constexpr int RED_WARPS = 8;
+constexpr int RS_STAGES = 6;
+constexpr int PAIR_M = 2 * BM;                          // 256 output rows per pair tile
+constexpr int HALF_N = BN / 2;                          // B columns held by each CTA
+constexpr int B_HALF_BYTES = BK * HALF_N * 2;           // 16 KiB: 2 chunks of 64 columns
+constexpr uint32_t PAIR_TX_BYTES = 2u * (A_STAGE_BYTES + B_HALF_BYTES);
 
 struct RsCtrl {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t tmem_full[2];
-    uint64_t tmem_empty[2];
+    uint64_t full[RS_STAGES];   // even CTA: both halves of a stage have landed
+    uint64_t empty[RS_STAGES];  // each CTA: the pair MMA is done with its stage
+    uint64_t tmem_full[2];      // each CTA: a partial is in its TMEM
+    uint64_t tmem_empty[2];     // even CTA: both CTAs' reductions consumed it
     uint64_t mma_done;
     uint32_t tmem_base;
     int32_t abort;
 };
 
 constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
-constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE_BYTES;
+constexpr int OFF_B = OFF_A + RS_STAGES * A_STAGE_BYTES;
+constexpr int OFF_EPI = OFF_B + RS_STAGES * B_HALF_BYTES;
 constexpr int OFF_CTRL = OFF_EPI + RED_WARPS * EPI_WARP_BYTES;
 constexpr int SMEM_ALLOC = OFF_CTRL + static_cast<int>(sizeof(RsCtrl)) + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget (227 KiB per CTA)");
+static_assert(OFF_B % 1024 == 0 && OFF_EPI % 1024 == 0, "swizzled buffers must be 1024-byte aligned");
 
 constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, /*B MN-major*/ true);
+constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, /*B MN-major*/ true);
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p)
 {
@@ -85,62 +97,77 @@ __device__ __forceinline__ bool red_bar_and(bool v)
     return r != 0;
 }
 
-// Output tiles of this CTA: q = c + i*G (row tiles of the full M, 256 columns).
-__device__ __forceinline__ int n_tiles_of(const RsParams& p)
+// Pair tiles of this cluster: q = cid + i * nc (256-row tiles of the full M,
+// 256 columns), the same sequence in both CTAs.
+struct PairSched {
+    int cid, nc, nt;
+};
+
+__device__ __forceinline__ PairSched pair_sched(const RsParams& p)
 {
+    PairSched s;
+    s.cid = static_cast<int>(cluster_id_x());
+    s.nc = static_cast<int>(nclusters_x());
     const int T = p.T_M * p.T_N;
-    const int c = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
-    return c < T ? (T - c + G - 1) / G : 0;
+    s.nt = s.cid < T ? (T - s.cid + s.nc - 1) / s.nc : 0;
+    return s;
 }
 
-__device__ void rs_loader(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, const ErrCtx& ec)
+__device__ void rs_loader(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, const ErrCtx& ec,
+                          uint32_t crank)
 {
     const uint32_t lane = lane_id();
-    const int c = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
+    const PairSched ps = pair_sched(p);
     const int KB = (p.K_r + BK - 1) / BK;
-    const int nt = n_tiles_of(p);
     uint32_t stage = 0, sphase = 0, filled = 0, last_par = 0;
     bool ok = true;
-    for (int i = 0; i < nt && ok; ++i) {
-        const int q = c + i * G;
-        const int m0 = (q / p.T_N) * BM, n0 = (q % p.T_N) * BN;
+    for (int i = 0; i < ps.nt && ok; ++i) {
+        const int q = ps.cid + i * ps.nc;
+        const int m0 = (q / p.T_N) * PAIR_M + static_cast<int>(crank) * BM;
+        const int n0 = (q % p.T_N) * BN + static_cast<int>(crank) * HALF_N;
         for (int r = 0; r < p.R && ok; ++r) {
             for (int kb = 0; kb < KB; ++kb) {
                 if (!wait_bar(&ctrl->empty[stage], sphase ^ 1u, ec, SITE_LOADER_EMPTY)) { ok = false; break; }
                 if (lane == 0) {
-                    uint64_t* fb = &ctrl->full[stage];
-                    mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
-                    tma_load_2d(smem + OFF_A + stage * A_STAGE_BYTES, &p.a_load[r], fb, kb * BK, m0);
-                    uint8_t* bs = smem + OFF_B + stage * B_STAGE_BYTES;
+                    // The even CTA's `full` barrier counts the bytes of both halves.
+                    const uint32_t fb = mapa_shared(smem_u32(&ctrl->full[stage]), 0);
+                    if (crank == 0) mbar_arrive_expect_tx(&ctrl->full[stage], PAIR_TX_BYTES);
+                    tma_load_2d_pair(smem + OFF_A + stage * A_STAGE_BYTES, &p.a_load[r], fb, kb * BK, m0);
+                    uint8_t* bs = smem + OFF_B + stage * B_HALF_BYTES;
 #pragma unroll
-                    for (int j = 0; j < BN / 64; ++j)
-                        tma_load_2d(bs + j * B_CHUNK_BYTES, &p.b_load[r], fb, n0 + 64 * j, kb * BK);
+                    for (int j = 0; j < HALF_N / 64; ++j)
+                        tma_load_2d_pair(bs + j * B_CHUNK_BYTES, &p.b_load[r], fb, n0 + 64 * j, kb * BK);
                 }
                 __syncwarp();
                 filled |= 1u << stage;
                 last_par = (last_par & ~(1u << stage)) | (sphase << stage);
-                if (++stage == STAGES) { stage = 0; sphase ^= 1u; }
+                if (++stage == RS_STAGES) { stage = 0; sphase ^= 1u; }
             }
         }
     }
-    for (int st = 0; st < STAGES; ++st)
-        if (filled & (1u << st)) drain_bar(&ctrl->full[st], (last_par >> st) & 1u, ec);
+    // The even CTA's `full` phases cover both CTAs' loads: let every armed
+    // one complete before the pair may exit.
+    if (crank == 0)
+        for (int st = 0; st < RS_STAGES; ++st)
+            if (filled & (1u << st)) drain_bar(&ctrl->full[st], (last_par >> st) & 1u, ec);
 }
 
+// Even CTA only.
 __device__ void rs_mma(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32_t tmem,
                        const ErrCtx& ec)
 {
     const uint32_t lane = lane_id();
+    const PairSched ps = pair_sched(p);
     const int KB = (p.K_r + BK - 1) / BK;
-    const int nt = n_tiles_of(p);
     const uint32_t a_base = smem_u32(smem + OFF_A);
     const uint32_t b_base = smem_u32(smem + OFF_B);
     uint32_t stage = 0, sphase = 0, acc = 0, aphase = 0;
     bool ok = true;
-    for (int i = 0; i < nt && ok; ++i) {
+    for (int i = 0; i < ps.nt && ok; ++i) {
         for (int r = 0; r < p.R && ok; ++r) {
-            // a fresh accumulator for each rank's partial
-            if (!wait_bar(&ctrl->tmem_empty[acc], aphase ^ 1u, ec, SITE_MMA_TMEM_EMPTY)) { ok = false; break; }
+            // a fresh accumulator for each rank's partial, once both CTAs'
+            // reductions have read the previous contents
+            if (!wait_bar_cluster(&ctrl->tmem_empty[acc], aphase ^ 1u, ec, SITE_MMA_TMEM_EMPTY)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d = tmem + acc * BN;
             for (int kb = 0; kb < KB; ++kb) {
@@ -148,44 +175,46 @@ __device__ void rs_mma(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32_t 
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t as = a_base + stage * A_STAGE_BYTES;
-                    const uint32_t bs = b_base + stage * B_STAGE_BYTES;
+                    const uint32_t bs = b_base + stage * B_HALF_BYTES;
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         const uint64_t ad = sdesc_sw128(as + k * (UMMA_K * 2), 16, 1024);
                         const uint64_t bd = sdesc_sw128(bs + k * (UMMA_K * 128), B_CHUNK_BYTES, 1024);
-                        mma_bf16(d, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                        mma_bf16_pair(d, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
                     }
-                    mma_commit(&ctrl->empty[stage]);
+                    mma_commit_pair(&ctrl->empty[stage], 0x3);  // both CTAs' stage is free
                 }
                 __syncwarp();
-                if (++stage == STAGES) { stage = 0; sphase ^= 1u; }
+                if (++stage == RS_STAGES) { stage = 0; sphase ^= 1u; }
             }
             if (!ok) break;
-            if (lane == 0) mma_commit(&ctrl->tmem_full[acc]);  // partial P_r is ready
+            if (lane == 0) mma_commit_pair(&ctrl->tmem_full[acc], 0x3);  // partial P_r is ready
             __syncwarp();
             if (++acc == 2) { acc = 0; aphase ^= 1u; }
         }
     }
-    if (lane == 0) mma_commit(&ctrl->mma_done);
+    if (lane == 0) mma_commit_pair(&ctrl->mma_done, 0x1);
     __syncwarp();
     drain_bar(&ctrl->mma_done, 0, ec);
 }
 
 __device__ void rs_reduce(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32_t tmem,
-                          const ErrCtx& ec, int warp)
+                          const ErrCtx& ec, int warp, uint32_t crank)
 {
     const uint32_t lane = lane_id();
-    const int c = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
+    const PairSched ps = pair_sched(p);
     const int quarter = warp & 3;
     const int half = (warp - 4) >> 2;
-    const int nt = n_tiles_of(p);
     uint8_t* buf = smem + OFF_EPI + (warp - 4) * EPI_WARP_BYTES;
     const uint32_t row_addr = smem_u32(buf) + lane * 128u;
+    uint32_t empty_caddr[2];
+    for (int a = 0; a < 2; ++a) empty_caddr[a] = mapa_shared(smem_u32(&ctrl->tmem_empty[a]), 0);
     uint32_t acc = 0, aphase = 0;
-    for (int i = 0; i < nt; ++i) {
+    for (int i = 0; i < ps.nt; ++i) {
         bool ok = true;
-        const int q = c + i * G;
-        const int m0 = (q / p.T_N) * BM, n0 = (q % p.T_N) * BN;
+        const int q = ps.cid + i * ps.nc;
+        const int m0 = (q / p.T_N) * PAIR_M + static_cast<int>(crank) * BM;
+        const int n0 = (q % p.T_N) * BN;
         float S[128];
 #pragma unroll
         for (int e = 0; e < 128; ++e) S[e] = 0.0f;
@@ -204,15 +233,18 @@ __device__ void rs_reduce(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctrl->tmem_empty[acc]);  // partial consumed
+            if (lane == 0) mbar_arrive_cluster(empty_caddr[acc]);  // partial consumed
             if (++acc == 2) { acc = 0; aphase ^= 1u; }
         }
 
-        // Scatter: these rows belong to rank j; store them in its slice.
-        const int j = m0 / p.Mb;
+        // Scatter: these rows belong to rank j; store them in its slice.  In a
+        // ragged last pair tile the odd CTA's rows may lie past M: it reduced
+        // zeros and stores nothing.
+        const bool rows_in = m0 < p.M;
+        const int j = rows_in ? m0 / p.Mb : 0;
         const int row_in_block = m0 - j * p.Mb + quarter * 32;
 #pragma unroll
-        for (int ch = 0; ch < 2 && ok; ++ch) {
+        for (int ch = 0; ch < 2 && ok && rows_in; ++ch) {
             uint32_t w[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
@@ -238,7 +270,7 @@ __device__ void rs_reduce(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32
         if (lane == 0) bulk_wait<0>();
         __syncwarp();
         if (!red_bar_and(ok)) break;
-        if (warp == 4 && lane == 0) {
+        if (warp == 4 && lane == 0 && rows_in) {
             fence_async_global();
             const int mt = (m0 - j * p.Mb) / 128;
             for (int t = 0; t < BN / 128; ++t) {
@@ -262,45 +294,54 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
     uint8_t* smem = align1024(smem_raw);
     RsCtrl* ctrl = reinterpret_cast<RsCtrl*>(smem + OFF_CTRL);
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
+    const uint32_t crank = cluster_ctarank();
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < STAGES; ++i) {
+        for (int i = 0; i < RS_STAGES; ++i) {
             mbar_init(&ctrl->full[i], 1);
             mbar_init(&ctrl->empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctrl->tmem_full[i], 1);
-            mbar_init(&ctrl->tmem_empty[i], RED_WARPS);
+            mbar_init(&ctrl->tmem_empty[i], 2 * RED_WARPS);
         }
         mbar_init(&ctrl->mma_done, 1);
+        // A device error latched by an earlier launch: do nothing.
         ctrl->abort = ld_relaxed_s32(p.status) != 0 ? 1 : 0;
         fence_barrier_init();
     }
-    __syncthreads();
-    if (ctrl->abort) return;
+    // Both CTAs' barriers exist before either CTA signals the other's.
+    cluster_sync();
     if (warp == 2) {
-        tmem_alloc(&ctrl->tmem_base, TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc_pair(&ctrl->tmem_base, TMEM_COLS);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
     const ErrCtx ec{p.status, &ctrl->abort, p.timeout_ns};
+    // The pair follows the even CTA's start-up decision, so both run or neither does.
+    const bool skip = ld_shared_cluster_u32(mapa_shared(smem_u32(&ctrl->abort), 0)) != 0;
 
-    if (warp == 0) {
-        rs_loader(p, smem, ctrl, ec);
-    } else if (warp == 1) {
-        rs_mma(p, smem, ctrl, tmem, ec);
-    } else if (warp >= 4) {
-        rs_reduce(p, smem, ctrl, tmem, ec, warp);
+    if (!skip) {
+        if (warp == 0) {
+            rs_loader(p, smem, ctrl, ec, crank);
+        } else if (warp == 1) {
+            if (crank == 0) rs_mma(p, smem, ctrl, tmem, ec);
+        } else if (warp >= 4) {
+            rs_reduce(p, smem, ctrl, tmem, ec, warp, crank);
+        }
     }
 
+    // No CTA of the pair leaves (or frees TMEM) while the other may still
+    // use its shared memory, barriers or TMEM.
     tc_fence_before();
     __syncthreads();
+    cluster_sync();
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tmem_dealloc_pair(tmem, TMEM_COLS);
     }
 }
 
@@ -308,7 +349,36 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
 
 size_t rs_smem_bytes() { return SMEM_ALLOC; }
 
-cudaError_t launch_gemm_rs(const RsParams& p, int grid, cudaStream_t s)
+// Clusters of this kernel that can be resident at once (0 on error).
+int rs_max_pairs()
+{
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] > 0) return cached[dev];
+    if (cudaFuncSetAttribute(gemm_rs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_ALLOC) != cudaSuccess)
+        return 0;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+    cfg.blockDim = dim3(RS_THREADS);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_rs_kernel, &cfg) != cudaSuccess) return 0;
+    cached[dev] = n;
+    return n;
+}
+
+cudaError_t launch_gemm_rs(const RsParams& p, int pairs, cudaStream_t s)
 {
     static bool attr_set[64] = {};
     int dev = 0;
@@ -322,13 +392,15 @@ cudaError_t launch_gemm_rs(const RsParams& p, int grid, cudaStream_t s)
         attr_set[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
     cfg.blockDim = dim3(RS_THREADS);
     cfg.dynamicSmemBytes = SMEM_ALLOC;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, gemm_rs_kernel, p);

@@ -415,8 +415,14 @@ opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t 
 
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != sig->device) return OPW_ERR_CUDA;
+    // CTAs work in pairs: num_ctas (or the SM count) is rounded down to an
+    // even number, at least 2, and capped at what can be resident.
     const int grid = grid_for(o, dev);
     if (grid <= 0) return OPW_ERR_CUDA;
+    const int max_pairs = rs_max_pairs();
+    if (max_pairs <= 0) return OPW_ERR_CUDA;
+    int pairs = grid / 2 > 0 ? grid / 2 : 1;
+    if (pairs > max_pairs) pairs = max_pairs;
 
     RsParams p;
     std::memset(&p, 0, sizeof p);
@@ -439,11 +445,11 @@ opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t 
     p.N = static_cast<int32_t>(N);
     p.K_r = static_cast<int32_t>(K_r);
     p.Mb = static_cast<int32_t>(Mb);
-    p.T_M = static_cast<int32_t>(M / BM);
+    p.T_M = static_cast<int32_t>((M + 2 * BM - 1) / (2 * BM));
     p.T_N = static_cast<int32_t>((N + BN - 1) / BN);
     p.T_fm = static_cast<int32_t>(Mb / 128);
     p.T_fn = static_cast<int32_t>((N + 127) / 128);
-    if (launch_gemm_rs(p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (launch_gemm_rs(p, pairs, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return OPW_ERR_CUDA;
     sig->epoch_last = epoch;
     return OPW_OK;

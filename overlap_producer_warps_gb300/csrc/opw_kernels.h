@@ -83,7 +83,7 @@ struct RsParams {
     uint64_t epoch;
     uint64_t timeout_ns;
     int32_t R, M, N, K_r, Mb;
-    int32_t T_M, T_N;
+    int32_t T_M, T_N;         // 256 x 256 pair tiles along M, along N
     int32_t T_fm, T_fn;       // 128x128 flag tiles per rank block along M, along N
 };
 
@@ -107,7 +107,8 @@ size_t rs_smem_bytes();
 
 // Launch helpers (cooperative launch so every CTA is co-resident).
 cudaError_t launch_ag_gemm(const AgParams& p, int grid, cudaStream_t s);
-cudaError_t launch_gemm_rs(const RsParams& p, int grid, cudaStream_t s);
+int rs_max_pairs();  // clusters of 2 GEMM-RS CTAs that fit at once (0 on error)
+cudaError_t launch_gemm_rs(const RsParams& p, int pairs, cudaStream_t s);
 cudaError_t launch_ring_allreduce(const RingParams& p, int sms, cudaStream_t s);
 
 }  // namespace opw

@@ -62,6 +62,25 @@ def test_shapes(api, R, M, K_r, N, order):
     _check_all(api, prob)
 
 
+@pytest.mark.parametrize("num_ctas", [1, 2, 5, 6])
+def test_pair_counts(api, num_ctas):
+    """CTAs run in pairs: 1 and 2 CTAs give one pair, 5 gives two.  With 15
+    pair tiles (M = 4 x 256 + 128, so the last row of pair tiles is ragged)
+    every pair does several tiles and one CTA of each last-row pair holds
+    rows past M."""
+    R, M, K_r, N = 3, 1152, 192, 768
+    d = inputs.rs_inputs(_cfg(R, M, K_r, N), seed=41 + num_ctas)
+    prob = RsProblem(d)
+    F = api.rs_num_flags(R, M, N)
+    sig = api.Signal(F)
+    e = sig.next_epoch()
+    prob.run(api, sig, e, api.make_opts(num_ctas=num_ctas))
+    st = sig.status()
+    assert st[0] == api.OK, st
+    assert np.array_equal(sig.flags().cpu().numpy(), oracle.expected_flags(F, e))
+    _check_all(api, prob)
+
+
 def test_deterministic_and_epochs(api):
     R, M, K_r, N = 4, 512, 256, 512
     d = inputs.rs_inputs(_cfg(R, M, K_r, N), seed=31)
