@@ -171,7 +171,10 @@ typedef struct {
     int32_t sync_mode;            /* OPW_SYNC_* */
     int32_t schedule;             /* OPW_SCHED_* */
     int32_t role;                 /* OPW_ROLE_* */
-    int32_t num_ctas;             /* persistent grid size; 0 = one CTA per SM */
+    int32_t num_ctas;             /* persistent grid size; 0 = one CTA per SM.  AG-GEMM
+                                     and GEMM-RS run CTAs in pairs (clusters of 2): the
+                                     count is rounded down to an even number, at least 2,
+                                     and capped at the pairs that can be resident. */
     const int32_t* publish_perm;  /* host [R] or NULL: rank publish_perm[i] is published
                                      i-th, and none of its tiles before every tile of
                                      rank publish_perm[i-1] is published.  NULL: ranks
@@ -209,11 +212,13 @@ int64_t opw_ag_num_row_counters(int32_t R, int64_t M_r, int64_t K);
  *   [F, 2F)           earliest time a consumer's acquire of the slot
  *                     succeeded (atomicMin; the caller fills this range
  *                     with all-ones bits before the launch)
- *   [2F, 2F+T)        per output tile: (cta << 32) | visit position
- *   [2F+T, 2F+2T)     per output tile: time the loader began it (before its
- *                     first flag acquire)
+ *   [2F, 2F+T)        per 256x256 output tile q = (row / 256) * ceil(N/256)
+ *                     + col / 256: (pair << 32) | visit position, where
+ *                     pair c is the CTA pair 2c, 2c+1
+ *   [2F+T, 2F+2T)     per output tile: time its pair's scheduler claimed it
+ *                     (before its first flag acquire)
  *   [2F+2T, 2F+2T+G)  per CTA: start time
- * with F = opw_ag_num_flags(), T = ceil(M/128)*ceil(N/256), G = grid size
+ * with F = opw_ag_num_flags(), T = ceil(M/256)*ceil(N/256), G = grid size
  * (at most OPW_TRACE_MAX_CTAS words are reserved).
  */
 #define OPW_TRACE_MAX_CTAS 1024
@@ -236,9 +241,10 @@ int64_t opw_ag_trace_words(int32_t R, int64_t M_r, int64_t N, int64_t K);
  *
  * Producer warps copy each flag tile of each A_r into G with TMA, wait for the
  * copy to complete, then publish flags[slot] = epoch with a .gpu release.
- * Consumer warps acquire each flag (>= epoch) before their TMA loads read that
- * tile of G, then run tcgen05 MMAs with TMEM accumulators.  After the launch
- * every flag slot holds `epoch` and G is bit-identical to the concatenation.
+ * Consumers, in CTA pairs working on 256x256 output tiles, acquire each flag
+ * (>= epoch) before their TMA loads read that tile of G, then run tcgen05
+ * cta_group::2 MMAs with TMEM accumulators.  After the launch every flag slot
+ * holds `epoch` and G is bit-identical to the concatenation.
  *
  * Shapes: M_r, K multiples of 64 (flag tile 64) or 128; N a multiple of 8;
  * R*M_r, N, K <= 2^31.  Alignment: heap_dev, B_dev, G_dev, C_dev, a_off and
@@ -307,10 +313,12 @@ int64_t opw_rs_num_flags(int32_t R, int64_t M, int64_t N);
  *   B_r   = [K_r, N] bf16 at heap_dev + rank_off[r] + b_off
  *   out_j = [M/R, N] bf16 at heap_dev + rank_off[j] + out_off
  *
- * The MMA warp produces partial tiles into a double-buffered TMEM accumulator
- * and signals each on an on-chip barrier; the reduction warps add them in
- * rank order as they land, write each finished row block to its rank, and
- * publish flags[slot] = epoch (.gpu release) per 128x128 output tile.
+ * CTA pairs work on 256x256 output tiles.  The pair's MMA (tcgen05
+ * cta_group::2) produces partial tiles into a double-buffered TMEM
+ * accumulator and signals each on an on-chip barrier; the reduction warps of
+ * both CTAs add them in rank order as they land, write each finished row
+ * block to its rank, and publish flags[slot] = epoch (.gpu release) per
+ * 128x128 output tile.
  *
  * Shapes: M a multiple of 128*R; K_r a multiple of 64; N a multiple of 8.
  * Alignment and errors as for opw_ag_gemm.  `opts` fields used: timeout_ns,

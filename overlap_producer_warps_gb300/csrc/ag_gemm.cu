@@ -7,40 +7,52 @@
 // Data Dependency") and computes at once (step 3); consumers start on their
 // own rank's rows and rotate ("Threadblock Swizzling").
 //
-// One CTA per SM, 8 warps:
-//   warp 0     loader: takes tiles from the on-chip tile queue and TMA-loads
-//              their A k-blocks from the gathered buffer G and B k-blocks into
-//              a 4-stage shared-memory ring: a plain GEMM pipeline.
-//   warp 1     MMA: one thread issues tcgen05.mma (bf16 x bf16 -> fp32) into a
-//              double-buffered TMEM accumulator (2 x 128 lanes x 256 columns).
-//   warp 2     gather producer: TMA-copies flag tiles of A_r into G through
-//              shared memory, waits for the copy to complete, and publishes the
-//              tile's flag with st.release.gpu.
-//   warp 3     allocates / frees TMEM; in between it is the scheduler: it
-//              picks the next output tile, acquires (ld.acquire.gpu) the flags
-//              of all the A tiles that output tile needs, and only then puts
-//              it on the tile queue.  Acquiring ahead of the loader keeps every
-//              global-memory round trip off the k-block loop.
-//   warps 4-7  epilogue: tcgen05.ld -> bf16 (round to nearest even) ->
-//              swizzled shared memory -> TMA store of C.
+// CTAs work in pairs (clusters of 2) on 256 x 256 output tiles with one
+// tcgen05 cta_group::2 MMA: CTA c of the pair holds rows 128c..128c+127 of
+// the tile's A rows and columns 128c..128c+127 of B in its shared memory and
+// receives its 128 accumulator rows in its own TMEM.  8 warps per CTA:
+//   warp 0     loader (both CTAs): takes tiles from the on-chip tile queue and
+//              TMA-loads this CTA's half of their A k-blocks (from the gathered
+//              buffer G) and B k-blocks into a 6-stage ring; the bytes of both
+//              halves complete on the even CTA's `full` barrier.
+//   warp 1     MMA (even CTA only): one thread issues the pair's tcgen05.mma
+//              (bf16 x bf16 -> fp32) into a double-buffered TMEM accumulator
+//              (2 x 128 lanes x 256 columns in each CTA).
+//   warp 2     gather producer (every CTA): TMA-copies flag tiles of A_r into G
+//              through shared memory, waits for the copy to complete, and
+//              publishes the tile's flag with st.release.gpu.
+//   warp 3     allocates / frees the pair's TMEM; in the even CTA it is also
+//              the scheduler: it picks the next output tile, acquires
+//              (ld.acquire.gpu) the flags of all the A rows that tile needs,
+//              and only then puts it on both CTAs' tile queues.  Acquiring
+//              ahead of the loaders keeps every global-memory round trip off
+//              the k-block loop.
+//   warps 4-7  epilogue (both CTAs): tcgen05.ld -> bf16 (round to nearest
+//              even) -> swizzled shared memory -> TMA store of C.
 // Every wait is bounded: on timeout the kernel latches an error in the
 // signal object's status word, drains its own in-flight copies and MMAs,
-// frees TMEM and returns.
+// frees TMEM and returns.  Cluster barriers bracket the kernel, so neither CTA
+// of a pair leaves while the other may still use its shared memory or TMEM.
 #include "opw_device.cuh"
 #include "opw_kernels.h"
 
 namespace opw {
 namespace {
 
+constexpr int AG_STAGES = 6;
+constexpr int HALF_N = BN / 2;                  // B columns held by each CTA
+constexpr int B_HALF_BYTES = BK * HALF_N * 2;   // 16 KiB: 2 chunks of 64 columns
+constexpr uint32_t PAIR_TX_BYTES = 2u * (A_STAGE_BYTES + B_HALF_BYTES);
+
 struct AgCtrl {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t tmem_full[2];
-    uint64_t tmem_empty[2];
+    uint64_t full[AG_STAGES];   // even CTA: both halves of a stage have landed
+    uint64_t empty[AG_STAGES];  // each CTA: the pair MMA is done with its stage
+    uint64_t tmem_full[2];      // each CTA: an accumulator is complete in its TMEM
+    uint64_t tmem_empty[2];     // even CTA: both CTAs' epilogues have read it
     uint64_t gfull[2];
-    uint64_t tq_full[TILE_Q];
-    uint64_t tq_empty[TILE_Q];
-    uint64_t need_next;  // loader -> scheduler: claim the next tile now
+    uint64_t tq_full[TILE_Q];   // each CTA: a tile id is in its queue slot
+    uint64_t tq_empty[TILE_Q];  // even CTA: every reader of the slot, in both CTAs, is done
+    uint64_t need_next;         // even CTA, loader -> scheduler: claim the next tile now
     uint64_t mma_done;
     int32_t tile_q[TILE_Q];
     uint32_t tmem_base;
@@ -48,8 +60,8 @@ struct AgCtrl {
 };
 
 constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
-constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE_BYTES;
+constexpr int OFF_B = OFF_A + AG_STAGES * A_STAGE_BYTES;
+constexpr int OFF_EPI = OFF_B + AG_STAGES * B_HALF_BYTES;
 constexpr int OFF_GATHER = OFF_EPI + 4 * EPI_WARP_BYTES;
 constexpr int OFF_CTRL = OFF_GATHER + 2 * GATHER_BUF_BYTES;
 constexpr int SMEM_ALLOC = OFF_CTRL + static_cast<int>(sizeof(AgCtrl)) + 1024;
@@ -58,14 +70,18 @@ static_assert(OFF_B % 1024 == 0 && OFF_EPI % 1024 == 0 && OFF_GATHER % 1024 == 0
               "swizzled buffers must be 1024-byte aligned");
 
 // The loader asks for its next tile this many k-blocks before the end of the
-// current one: late enough that a CTA never holds more than one tile it has
-// not started (the dynamic schedule stays greedy, so CTAs that wait longer on
+// current one: late enough that a pair never holds more than one tile it has
+// not started (the dynamic schedule stays greedy, so pairs that wait longer on
 // the gather do not end up with fewer tiles), early enough to hide the flag
 // acquire and the first TMA loads.
 constexpr int CLAIM_LEAD_KB = 64;
 
+// Readers of each tile-queue slot: loader, MMA and 4 epilogue warps of the
+// even CTA, loader and 4 epilogue warps of the odd one.
+constexpr uint32_t TQ_READERS = 1 + 1 + 4 + 1 + 4;
+
 constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators of 256 columns
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, /*B MN-major*/ true);
+constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, /*B MN-major*/ true);
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p)
 {
@@ -86,12 +102,12 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, const 
     }
 }
 
-// Tile visited at position `idx` of the dynamic schedule.  Output row tiles
-// are taken in the order their flag tiles are published, in groups of
-// p.group_rows rows; within a group the column index runs slowest, so when B
-// is larger than L2 can hold next to everything else, the CTAs working at
-// the same time share B column tiles instead of streaming all of B for
-// every few rows (group_rows = 1 when B fits).
+// Pair tile visited at position `idx` of the dynamic schedule.  Rows of pair
+// tiles (256 rows) are taken in the order their flag tiles are published, in
+// groups of p.group_rows rows; within a group the column index runs slowest,
+// so when B is larger than L2 can hold next to everything else, the pairs
+// working at the same time share B column tiles instead of streaming all of B
+// for every few rows (group_rows = 1 when B fits).
 __device__ __forceinline__ int ready_tile(const AgParams& p, int idx)
 {
     const int GM = p.group_rows;
@@ -102,8 +118,8 @@ __device__ __forceinline__ int ready_tile(const AgParams& p, int idx)
     const int mp = first + local % rows;
     const int n = local / rows;
     int m = mp;
-    if (p.ft == BM && p.M_r % BM == 0) {
-        const int tpr = p.M_r / BM;
+    if (p.ft == BM && p.M_r % PAIR_M == 0) {
+        const int tpr = p.M_r / PAIR_M;
         if (p.has_perm) {
             m = p.perm[mp / tpr] * tpr + mp % tpr;
         } else {
@@ -222,7 +238,7 @@ __device__ __noinline__ bool acquire_flags(const AgParams& p, const ErrCtx& ec, 
     }
 }
 
-// ------------------------------------------------------------------ loader
+// ------------------------------------------------------------------ scheduler
 
 // Flag rows covered by output rows [m0, m0 + BM): one for 128-row flag tiles,
 // two for 64-row ones (base1 = -1 when there is no second row).
@@ -244,40 +260,56 @@ struct LoaderRing {
     uint32_t stage = 0, sphase = 0, filled = 0, last_par = 0;
 };
 
-// Issue the TMA loads of k-blocks [kb0, kb1) of tile (m0, n0): the plain
-// GEMM pipeline, with nothing else in the loop.
+// Issue the TMA loads of this CTA's half of k-blocks [kb0, kb1) of a pair
+// tile (A rows from m0, B columns from n0): the plain GEMM pipeline, with
+// nothing else in the loop.
 __device__ __forceinline__ bool issue_kblocks(const AgParams& p, uint8_t* smem, AgCtrl* ctrl,
                                               const ErrCtx& ec, LoaderRing& rg, int m0, int n0,
-                                              int kb0, int kb1)
+                                              int kb0, int kb1, uint32_t crank)
 {
     const uint32_t lane = lane_id();
     for (int kb = kb0; kb < kb1; ++kb) {
         if (!wait_bar(&ctrl->empty[rg.stage], rg.sphase ^ 1u, ec, SITE_LOADER_EMPTY)) return false;
         if (lane == 0) {
-            uint64_t* fb = &ctrl->full[rg.stage];
-            mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
-            tma_load_2d(smem + OFF_A + rg.stage * A_STAGE_BYTES, &p.g_load, fb, kb * BK, m0);
-            uint8_t* bs = smem + OFF_B + rg.stage * B_STAGE_BYTES;
+            const uint32_t fb = mapa_shared(smem_u32(&ctrl->full[rg.stage]), 0);
+            if (crank == 0) mbar_arrive_expect_tx(&ctrl->full[rg.stage], PAIR_TX_BYTES);
+            tma_load_2d_pair(smem + OFF_A + rg.stage * A_STAGE_BYTES, &p.g_load, fb, kb * BK, m0);
+            uint8_t* bs = smem + OFF_B + rg.stage * B_HALF_BYTES;
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-                tma_load_2d(bs + j * B_CHUNK_BYTES, &p.b_load, fb, n0 + 64 * j, kb * BK);
+            for (int j = 0; j < HALF_N / 64; ++j)
+                tma_load_2d_pair(bs + j * B_CHUNK_BYTES, &p.b_load, fb, n0 + 64 * j, kb * BK);
         }
         __syncwarp();
         rg.filled |= 1u << rg.stage;
         rg.last_par = (rg.last_par & ~(1u << rg.stage)) | (rg.sphase << rg.stage);
-        if (++rg.stage == STAGES) { rg.stage = 0; rg.sphase ^= 1u; }
+        if (++rg.stage == AG_STAGES) { rg.stage = 0; rg.sphase ^= 1u; }
     }
     return true;
 }
 
+// Take the next tile id from this CTA's queue and release the slot on the
+// even CTA's tq_empty (-2 when the wait failed).
+__device__ __forceinline__ int pop_tile(AgCtrl* ctrl, const ErrCtx& ec, uint32_t& tq,
+                                        uint32_t& tqphase)
+{
+    if (!wait_bar_cluster(&ctrl->tq_full[tq], tqphase, ec, SITE_TILE_QUEUE)) return -2;
+    const int q = reinterpret_cast<volatile int32_t*>(ctrl->tile_q)[tq];
+    __syncwarp();
+    if (lane_id() == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctrl->tq_empty[tq]), 0));
+    __syncwarp();
+    if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
+    return q;
+}
+
+// Even CTA, warp 3.
 __device__ void run_scheduler(const AgParams& p, AgCtrl* ctrl, const ErrCtx& ec)
 {
     const uint32_t lane = lane_id();
-    const int G = static_cast<int>(gridDim.x);
-    const int c = static_cast<int>(blockIdx.x);
+    const int G = static_cast<int>(nclusters_x());
+    const int c = static_cast<int>(cluster_id_x());
     const int T = p.T_M * p.T_N;
 
-    // Static schedule: this CTA owns tiles q = c + i*G; it starts at the first
+    // Static schedule: this pair owns tiles q = c + i*G; it starts at the first
     // one in its home rank's rows (h*tiles_per_pe row tiles down) and wraps.
     const int n_mine = c < T ? (T - c + G - 1) / G : 0;
     const int h = c % p.R;
@@ -285,14 +317,17 @@ __device__ void run_scheduler(const AgParams& p, AgCtrl* ctrl, const ErrCtx& ec)
     int i0 = start_q <= c ? 0 : static_cast<int>((start_q - c + G - 1) / G);
     if (i0 >= n_mine) i0 = 0;
 
+    const uint32_t peer_tq_full0 = mapa_shared(smem_u32(&ctrl->tq_full[0]), 1);
+    const uint32_t peer_tile_q0 = mapa_shared(smem_u32(&ctrl->tile_q[0]), 1);
     uint32_t tq = 0, tqphase = 0;
     bool serial_pending = (p.sync_mode == OPW_SYNC_SERIAL);
     for (int s = 0;; ++s) {
         // Claim tile s only when the loader asks for it (it has reached the
         // last CLAIM_LEAD_KB k-blocks of tile s-1; phases cannot alias, since
-        // the loader has popped at most s tiles) and a queue slot is free.
+        // the loader has popped at most s tiles) and the queue slot is free
+        // in both CTAs.
         if (s > 0 && !wait_bar(&ctrl->need_next, (s - 1) & 1u, ec, SITE_TILE_QUEUE)) return;
-        if (!wait_bar(&ctrl->tq_empty[tq], tqphase ^ 1u, ec, SITE_TILE_QUEUE)) return;
+        if (!wait_bar_cluster(&ctrl->tq_empty[tq], tqphase ^ 1u, ec, SITE_TILE_QUEUE)) return;
         int q;
         if (p.schedule == OPW_SCHED_READY) {
             long long idx = 0;
@@ -313,21 +348,28 @@ __device__ void run_scheduler(const AgParams& p, AgCtrl* ctrl, const ErrCtx& ec)
                 if (!wait_all_published(p, ec)) return;
                 serial_pending = false;
             }
-            // Acquire: no load of this tile's A rows before all their flags show the epoch.
-            int base0, base1;
-            flag_rows(p, (q / p.T_N) * BM, base0, base1);
-            int ready_kt = 0;
-            while (ready_kt < p.T_k)
-                if (!acquire_flags(p, ec, base0, base1, ready_kt)) return;
-            // every lane's acquire precedes lane 0's release through the queue
+            // Acquire: no load of this tile's A rows (both 128-row halves)
+            // before all their flags show the epoch.
+            for (int half = 0; half < 2; ++half) {
+                const int m0 = (q / p.T_N) * PAIR_M + half * BM;
+                if (m0 >= p.M) break;
+                int base0, base1;
+                flag_rows(p, m0, base0, base1);
+                int ready_kt = 0;
+                while (ready_kt < p.T_k)
+                    if (!acquire_flags(p, ec, base0, base1, ready_kt)) return;
+            }
+            // every lane's acquire precedes lane 0's release through the queues
             __syncwarp();
             if (lane == 0) fence_acq_rel_gpu();
             __syncwarp();
         }
-        // Hand the tile over (-1 = no more work).
+        // Hand the tile over to both CTAs (-1 = no more work).
         if (lane == 0) {
             reinterpret_cast<volatile int32_t*>(ctrl->tile_q)[tq] = q;
-            mbar_arrive(&ctrl->tq_full[tq]);  // release: the acquires above come first
+            st_shared_cluster_s32(peer_tile_q0 + 4u * tq, q);
+            mbar_arrive(&ctrl->tq_full[tq]);                    // release: the acquires above come first
+            mbar_arrive_cluster(peer_tq_full0 + 8u * tq);
         }
         __syncwarp();
         if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
@@ -337,41 +379,40 @@ __device__ void run_scheduler(const AgParams& p, AgCtrl* ctrl, const ErrCtx& ec)
 
 // ------------------------------------------------------------------ loader
 
-// Warp 0: takes tiles from the queue (their flags already acquired) and
-// streams their k-blocks through the shared-memory ring.
-__device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const ErrCtx& ec)
+// Warp 0 of both CTAs: takes tiles from the queue (their flags already
+// acquired) and streams this CTA's half of their k-blocks through the ring.
+__device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const ErrCtx& ec,
+                           uint32_t crank)
 {
     const uint32_t lane = lane_id();
     const int KB = p.K / BK;
     LoaderRing rg;
     uint32_t tq = 0, tqphase = 0;
     while (true) {
-        if (!wait_bar(&ctrl->tq_full[tq], tqphase, ec, SITE_TILE_QUEUE)) break;
-        const int q = reinterpret_cast<volatile int32_t*>(ctrl->tile_q)[tq];
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(&ctrl->tq_empty[tq]);
-            // consume_token: the scheduler's flag acquires reach this thread
-            // through the queue barrier; order them before the async-proxy
-            // reads of the tile.
-            if (q >= 0) fence_async_global();
-        }
-        __syncwarp();
-        if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
+        const int q = pop_tile(ctrl, ec, tq, tqphase);
         if (q < 0) break;
-        const int m0 = (q / p.T_N) * BM, n0 = (q % p.T_N) * BN;
+        // consume_token: the scheduler's flag acquires reach this thread
+        // through the queue barrier; order them before the async-proxy
+        // reads of the tile.
+        if (lane == 0) fence_async_global();
+        __syncwarp();
+        const int m0 = (q / p.T_N) * PAIR_M + static_cast<int>(crank) * BM;
+        const int n0 = (q % p.T_N) * BN + static_cast<int>(crank) * HALF_N;
         const int kb_ask = KB > CLAIM_LEAD_KB ? KB - CLAIM_LEAD_KB : 0;
-        if (!issue_kblocks(p, smem, ctrl, ec, rg, m0, n0, 0, kb_ask)) break;
-        if (lane == 0) mbar_arrive(&ctrl->need_next);
-        if (!issue_kblocks(p, smem, ctrl, ec, rg, m0, n0, kb_ask, KB)) break;
+        if (!issue_kblocks(p, smem, ctrl, ec, rg, m0, n0, 0, kb_ask, crank)) break;
+        if (crank == 0 && lane == 0) mbar_arrive(&ctrl->need_next);
+        if (!issue_kblocks(p, smem, ctrl, ec, rg, m0, n0, kb_ask, KB, crank)) break;
     }
-    // Every TMA load this warp issued must land before the CTA may exit.
-    for (int st = 0; st < STAGES; ++st)
-        if (rg.filled & (1u << st)) drain_bar(&ctrl->full[st], (rg.last_par >> st) & 1u, ec);
+    // The even CTA's `full` phases cover both CTAs' loads: every armed one
+    // must complete before the pair may exit.
+    if (crank == 0)
+        for (int st = 0; st < AG_STAGES; ++st)
+            if (rg.filled & (1u << st)) drain_bar(&ctrl->full[st], (rg.last_par >> st) & 1u, ec);
 }
 
 // ------------------------------------------------------------------ MMA
 
+// Even CTA, warp 1.
 __device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t tmem,
                         const ErrCtx& ec)
 {
@@ -382,14 +423,11 @@ __device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t
     uint32_t stage = 0, sphase = 0, acc = 0, aphase = 0, tq = 0, tqphase = 0;
     bool ok = true;
     while (ok) {
-        if (!wait_bar(&ctrl->tq_full[tq], tqphase, ec, SITE_TILE_QUEUE)) break;
-        const int q = reinterpret_cast<volatile int32_t*>(ctrl->tile_q)[tq];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctrl->tq_empty[tq]);
-        if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
+        const int q = pop_tile(ctrl, ec, tq, tqphase);
         if (q < 0) break;
 
-        if (!wait_bar(&ctrl->tmem_empty[acc], aphase ^ 1u, ec, SITE_MMA_TMEM_EMPTY)) break;
+        // both CTAs' epilogues have read this accumulator
+        if (!wait_bar_cluster(&ctrl->tmem_empty[acc], aphase ^ 1u, ec, SITE_MMA_TMEM_EMPTY)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * BN;
         for (int kb = 0; kb < KB; ++kb) {
@@ -397,7 +435,7 @@ __device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t as = a_base + stage * A_STAGE_BYTES;
-                const uint32_t bs = b_base + stage * B_STAGE_BYTES;
+                const uint32_t bs = b_base + stage * B_HALF_BYTES;
 #pragma unroll
                 for (int k = 0; k < BK / UMMA_K; ++k) {
                     // A: K-major, rows 128 B apart, 8-row groups 1024 B apart;
@@ -406,43 +444,42 @@ __device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t
                     // B: N-major, 64-column chunks 8 KiB apart (LBO), 8-row K groups
                     //    1024 B apart (SBO); k steps of 16 rows advance 2 KiB.
                     const uint64_t bd = sdesc_sw128(bs + k * (UMMA_K * 128), B_CHUNK_BYTES, 1024);
-                    mma_bf16(d, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                    mma_bf16_pair(d, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
                 }
-                mma_commit(&ctrl->empty[stage]);  // frees the stage when these MMAs finish
+                mma_commit_pair(&ctrl->empty[stage], 0x3);  // frees both CTAs' stage when done
             }
             __syncwarp();
-            if (++stage == STAGES) { stage = 0; sphase ^= 1u; }
+            if (++stage == AG_STAGES) { stage = 0; sphase ^= 1u; }
         }
         if (!ok) break;
-        if (lane == 0) mma_commit(&ctrl->tmem_full[acc]);
+        if (lane == 0) mma_commit_pair(&ctrl->tmem_full[acc], 0x3);
         __syncwarp();
         if (++acc == 2) { acc = 0; aphase ^= 1u; }
     }
     // Every MMA issued must complete before TMEM is released.
-    if (lane == 0) mma_commit(&ctrl->mma_done);
+    if (lane == 0) mma_commit_pair(&ctrl->mma_done, 0x1);
     __syncwarp();
     drain_bar(&ctrl->mma_done, 0, ec);
 }
 
 // ------------------------------------------------------------------ epilogue
 
+// Warps 4-7 of both CTAs: this CTA's 128 rows of each pair tile.
 __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t tmem,
-                             const ErrCtx& ec, int warp)
+                             const ErrCtx& ec, int warp, uint32_t crank)
 {
     const uint32_t lane = lane_id();
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
     uint8_t* buf = smem + OFF_EPI + quarter * EPI_WARP_BYTES;
     const uint32_t row_addr = smem_u32(buf) + lane * 128u;
+    uint32_t empty_caddr[2];
+    for (int a = 0; a < 2; ++a) empty_caddr[a] = mapa_shared(smem_u32(&ctrl->tmem_empty[a]), 0);
     uint32_t acc = 0, aphase = 0, tq = 0, tqphase = 0;
     while (true) {
-        if (!wait_bar(&ctrl->tq_full[tq], tqphase, ec, SITE_TILE_QUEUE)) break;
-        const int q = reinterpret_cast<volatile int32_t*>(ctrl->tile_q)[tq];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctrl->tq_empty[tq]);
-        if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
+        const int q = pop_tile(ctrl, ec, tq, tqphase);
         if (q < 0) break;
 
-        const int m0 = (q / p.T_N) * BM;
+        const int m0 = (q / p.T_N) * PAIR_M + static_cast<int>(crank) * BM;
         const int n0 = (q % p.T_N) * BN;
         const int row0 = m0 + quarter * 32;
         if (!wait_bar(&ctrl->tmem_full[acc], aphase, ec, SITE_EPI_TMEM_FULL)) break;
@@ -456,10 +493,10 @@ __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uin
             tmem_ld_wait(v0);
             tmem_ld_wait(v1);
             if (ch == BN / 64 - 1) {
-                // accumulator fully read: the MMA warp may reuse it
+                // accumulator fully read: the MMA may reuse it
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctrl->tmem_empty[acc]);
+                if (lane == 0) mbar_arrive_cluster(empty_caddr[acc]);
             }
             uint32_t w[32];
 #pragma unroll
@@ -627,22 +664,23 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
     uint8_t* smem = align1024(smem_raw);
     AgCtrl* ctrl = reinterpret_cast<AgCtrl*>(smem + OFF_CTRL);
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
+    const uint32_t crank = cluster_ctarank();
     const bool consumer = p.role != OPW_ROLE_PRODUCER;
     const bool producer = p.role != OPW_ROLE_CONSUMER;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < STAGES; ++i) {
+        for (int i = 0; i < AG_STAGES; ++i) {
             mbar_init(&ctrl->full[i], 1);
             mbar_init(&ctrl->empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctrl->tmem_full[i], 1);
-            mbar_init(&ctrl->tmem_empty[i], 4);
+            mbar_init(&ctrl->tmem_empty[i], 2 * 4);  // 4 epilogue warps in each CTA
             mbar_init(&ctrl->gfull[i], 1);
         }
         for (int i = 0; i < TILE_Q; ++i) {
             mbar_init(&ctrl->tq_full[i], 1);
-            mbar_init(&ctrl->tq_empty[i], 1 + 1 + 4);  // loader, MMA, 4 epilogue warps
+            mbar_init(&ctrl->tq_empty[i], TQ_READERS);
         }
         mbar_init(&ctrl->need_next, 1);
         mbar_init(&ctrl->mma_done, 1);
@@ -650,12 +688,11 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
         ctrl->abort = ld_relaxed_s32(p.status) != 0 ? 1 : 0;
         fence_barrier_init();
     }
-    __syncthreads();
-    if (ctrl->abort) return;
-
+    // Both CTAs' barriers exist before either CTA signals the other's.
+    cluster_sync();
     if (warp == 3 && consumer) {
-        tmem_alloc(&ctrl->tmem_base, TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc_pair(&ctrl->tmem_base, TMEM_COLS);
+        tmem_relinquish_pair();
     }
     if (threadIdx.x == 32) {
         prefetch_tmap(&p.g_load);
@@ -674,54 +711,93 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
         const int T = p.T_M * p.T_N;
         if (blockIdx.x < OPW_TRACE_MAX_CTAS) p.trace[2 * F + 2 * T + blockIdx.x] = t_start;
     }
+    // The pair follows the even CTA's start-up decision, so both run or neither does.
+    const bool skip = ld_shared_cluster_u32(mapa_shared(smem_u32(&ctrl->abort), 0)) != 0;
 
-    if (warp == 0) {
-        if (consumer) run_loader(p, smem, ctrl, ec);
-    } else if (warp == 1) {
-        if (consumer) run_mma(p, smem, ctrl, tmem, ec);
-    } else if (warp == 2) {
-        if (producer) run_gather(p, smem, ctrl, ec, t_start);
-    } else if (warp == 3) {
-        if (consumer) run_scheduler(p, ctrl, ec);
-    } else if (warp >= 4) {
-        if (consumer) run_epilogue(p, smem, ctrl, tmem, ec, warp);
+    if (!skip) {
+        if (warp == 0) {
+            if (consumer) run_loader(p, smem, ctrl, ec, crank);
+        } else if (warp == 1) {
+            if (consumer && crank == 0) run_mma(p, smem, ctrl, tmem, ec);
+        } else if (warp == 2) {
+            if (producer) run_gather(p, smem, ctrl, ec, t_start);
+        } else if (warp == 3) {
+            if (consumer && crank == 0) run_scheduler(p, ctrl, ec);
+        } else {
+            if (consumer) run_epilogue(p, smem, ctrl, tmem, ec, warp, crank);
+        }
     }
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync();
     if (warp == 3 && consumer) {
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tmem_dealloc_pair(tmem, TMEM_COLS);
     }
+}
+
+cudaLaunchConfig_t pair_config(unsigned pairs, cudaStream_t s, cudaLaunchAttribute* attr)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2u * pairs);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    // Consumers wait on flags that other CTAs' producers publish: every CTA
+    // must be resident at once.
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cfg;
+}
+
+bool set_smem_attr()
+{
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(ag_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_ALLOC) != cudaSuccess)
+            return false;
+        attr_set[dev] = true;
+    }
+    return true;
 }
 
 }  // namespace
 
 size_t ag_smem_bytes() { return SMEM_ALLOC; }
 
-cudaError_t launch_ag_gemm(const AgParams& p, int grid, cudaStream_t s)
+int ag_max_pairs()
 {
-    static bool attr_set[64] = {};
+    static int cached[64] = {};
     int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        err = cudaFuncSetAttribute(ag_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   SMEM_ALLOC);
-        if (err != cudaSuccess) return err;
-        attr_set[dev] = true;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = SMEM_ALLOC;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] > 0) return cached[dev];
+    if (!set_smem_attr()) return 0;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = pair_config(static_cast<unsigned>(sms / 2), nullptr, attr);
+    cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, ag_gemm_kernel, &cfg) != cudaSuccess) return 0;
+    cached[dev] = n;
+    return n;
+}
+
+cudaError_t launch_ag_gemm(const AgParams& p, int pairs, cudaStream_t s)
+{
+    if (!set_smem_attr()) return cudaErrorInvalidDevice;
+    cudaLaunchAttribute attr[2];
+    const cudaLaunchConfig_t cfg = pair_config(static_cast<unsigned>(pairs), s, attr);
     return cudaLaunchKernelEx(&cfg, ag_gemm_kernel, p);
 }
 

@@ -161,6 +161,10 @@ extern "C" opw_status opw_ag_gemm_noalloc(const opw_symm* symm, size_t a_off, in
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
         return OPW_ERR_CUDA;
     const int grid = (o.num_ctas > 0 && o.num_ctas < sms) ? o.num_ctas : sms;
+    const int max_pairs = ag_max_pairs();
+    if (max_pairs <= 0) return OPW_ERR_CUDA;
+    int pairs = grid / 2 > 0 ? grid / 2 : 1;
+    if (pairs > max_pairs) pairs = max_pairs;
 
     int64_t* flags = static_cast<int64_t*>(scratch);
     unsigned long long* counters = static_cast<unsigned long long*>(scratch) + kMaxFlags;
@@ -193,13 +197,13 @@ extern "C" opw_status opw_ag_gemm_noalloc(const opw_symm* symm, size_t a_off, in
     p.ft = static_cast<int32_t>(ft);
     p.T_mr = static_cast<int32_t>(M_r / ft);
     p.T_k = static_cast<int32_t>(K / ft);
-    p.T_M = static_cast<int32_t>((M + BM - 1) / BM);
+    p.T_M = static_cast<int32_t>((M + PAIR_M - 1) / PAIR_M);
     p.T_N = static_cast<int32_t>((N + BN - 1) / BN);
     p.role = OPW_ROLE_FUSED;
     p.sync_mode = o.sync_mode;
     p.schedule = o.schedule;
     // Row groups only pay when B (K x N bf16) is too big to stay in L2.
-    p.group_rows = (K * N * 2 > (int64_t(64) << 20)) ? 16 : 1;
+    p.group_rows = (K * N * 2 > (int64_t(64) << 20)) ? 8 : 1;
     p.signal_mode = o.signal_mode;
     p.has_perm = o.publish_perm != nullptr;
     p.has_delay = o.delay_ns != nullptr;
@@ -216,6 +220,6 @@ extern "C" opw_status opw_ag_gemm_noalloc(const opw_symm* symm, size_t a_off, in
     if (blocks < 1) blocks = 1;
     noalloc_clear_kernel<<<blocks, 256, 0, st>>>(flags, F, counters, status_dev);
     if (cudaGetLastError() != cudaSuccess) return OPW_ERR_CUDA;
-    if (launch_ag_gemm(p, grid, st) != cudaSuccess) return OPW_ERR_CUDA;
+    if (launch_ag_gemm(p, pairs, st) != cudaSuccess) return OPW_ERR_CUDA;
     return OPW_OK;
 }

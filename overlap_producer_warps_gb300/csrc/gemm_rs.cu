@@ -37,7 +37,6 @@ namespace {
 constexpr int RS_THREADS = 384;
 constexpr int RED_WARPS = 8;
 constexpr int RS_STAGES = 6;
-constexpr int PAIR_M = 2 * BM;                          // 256 output rows per pair tile
 constexpr int HALF_N = BN / 2;                          // B columns held by each CTA
 constexpr int B_HALF_BYTES = BK * HALF_N * 2;           // 16 KiB: 2 chunks of 64 columns
 constexpr uint32_t PAIR_TX_BYTES = 2u * (A_STAGE_BYTES + B_HALF_BYTES);

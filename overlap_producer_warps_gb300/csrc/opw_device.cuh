@@ -367,6 +367,11 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t caddr)
     return v;
 }
 
+__device__ __forceinline__ void st_shared_cluster_s32(uint32_t caddr, int32_t v)
+{
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
+}
+
 // Every thread of both CTAs: release this CTA's shared-memory writes to the
 // cluster and wait for the other CTA.
 __device__ __forceinline__ void cluster_sync()

@@ -255,7 +255,7 @@ int64_t opw_ag_trace_words(int32_t R, int64_t M_r, int64_t N, int64_t K)
 {
     const int64_t F = opw_ag_num_flags(R, M_r, K);
     if (F < 0 || N <= 0) return -1;
-    const int64_t T = ((R * M_r + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int64_t T = ((R * M_r + PAIR_M - 1) / PAIR_M) * ((N + BN - 1) / BN);
     return 2 * F + 2 * T + OPW_TRACE_MAX_CTAS;
 }
 
@@ -310,8 +310,14 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
     // ---- launch
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != sig->device) return OPW_ERR_CUDA;
+    // CTAs work in pairs: num_ctas (or the SM count) is rounded down to an
+    // even number, at least 2, and capped at what can be resident.
     const int grid = grid_for(o, dev);
     if (grid <= 0) return OPW_ERR_CUDA;
+    const int max_pairs = ag_max_pairs();
+    if (max_pairs <= 0) return OPW_ERR_CUDA;
+    int pairs = grid / 2 > 0 ? grid / 2 : 1;
+    if (pairs > max_pairs) pairs = max_pairs;
 
     AgParams p;
     std::memset(&p, 0, sizeof p);
@@ -342,13 +348,13 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
     p.ft = static_cast<int32_t>(ft);
     p.T_mr = static_cast<int32_t>(M_r / ft);
     p.T_k = static_cast<int32_t>(K / ft);
-    p.T_M = static_cast<int32_t>((M + BM - 1) / BM);
+    p.T_M = static_cast<int32_t>((M + PAIR_M - 1) / PAIR_M);
     p.T_N = static_cast<int32_t>((N + BN - 1) / BN);
     p.role = o.role;
     p.sync_mode = o.sync_mode;
     p.schedule = o.schedule;
     // Row groups only pay when B (K x N bf16) is too big to stay in L2.
-    p.group_rows = (K * N * 2 > (int64_t(64) << 20)) ? 16 : 1;
+    p.group_rows = (K * N * 2 > (int64_t(64) << 20)) ? 8 : 1;
     p.signal_mode = o.signal_mode;
     p.has_perm = o.publish_perm != nullptr;
     p.has_delay = o.delay_ns != nullptr;
@@ -362,7 +368,7 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
     for (int r = 0; r < R; ++r)
         p.rank_target[r] = produces ? sig->rank_done[r] + per_rank : sig->rank_target_last[r];
 
-    if (launch_ag_gemm(p, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (launch_ag_gemm(p, pairs, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return OPW_ERR_CUDA;
 
     // ---- host bookkeeping for the next launch on this object
@@ -376,7 +382,7 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
         }
     }
     if (o.role != OPW_ROLE_PRODUCER && o.schedule == OPW_SCHED_READY)
-        sig->claim_next += static_cast<uint64_t>(p.T_M) * p.T_N + static_cast<uint64_t>(grid);
+        sig->claim_next += static_cast<uint64_t>(p.T_M) * p.T_N + static_cast<uint64_t>(pairs);
     return OPW_OK;
 }
 

@@ -11,17 +11,17 @@
 
 namespace opw {
 
-// GEMM tiling shared by both kernels (one CTA per SM, tcgen05 cta_group::1).
-constexpr int BM = 128;       // rows per output tile = TMEM lanes
+// GEMM tiling shared by both kernels: CTAs work in pairs (clusters of 2, one
+// CTA per SM, tcgen05 cta_group::2) on PAIR_M x BN output tiles.
+constexpr int BM = 128;       // output rows per CTA = TMEM lanes
+constexpr int PAIR_M = 2 * BM;  // output rows per pair tile
 constexpr int BN = 256;       // columns per output tile = fp32 TMEM columns per accumulator
 constexpr int BK = 64;        // K per pipeline stage = one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;    // K per tcgen05.mma (kind::f16)
-constexpr int STAGES = 4;     // A/B shared-memory ring depth
 constexpr int TILE_Q = 4;     // depth of the tile-id queue (loader -> MMA, epilogue)
 
 constexpr int A_STAGE_BYTES = BM * BK * 2;       // 16 KiB
 constexpr int B_CHUNK_BYTES = BK * 64 * 2;       // 8 KiB: 64 K-rows x 64 N-columns
-constexpr int B_STAGE_BYTES = BK * BN * 2;       // 32 KiB: 4 chunks
 constexpr int EPI_WARP_BYTES = 32 * 64 * 2;      // 4 KiB: 32 rows x 64 columns bf16
 constexpr int GATHER_SUB_ROWS = 32;              // producer copies a flag tile 32 rows at a time
 constexpr int GATHER_BUF_BYTES = GATHER_SUB_ROWS * 128 * 2;  // 8 KiB (flag tile <= 128 wide)
@@ -61,7 +61,7 @@ struct AgParams {
     int32_t R, M_r, M, N, K;
     int32_t ft;               // flag tile edge (64 or 128)
     int32_t T_mr, T_k;        // flag tiles per rank along M, along K
-    int32_t T_M, T_N;         // output tiles
+    int32_t T_M, T_N;         // PAIR_M x BN pair tiles along M, along N
     int32_t role, sync_mode, schedule;
     int32_t group_rows;       // dynamic schedule: row tiles per rasterisation group
     int32_t signal_mode;      // OPW_SIGNAL_TILE_SET or OPW_SIGNAL_ROW_ADD
@@ -106,7 +106,8 @@ size_t ag_smem_bytes();
 size_t rs_smem_bytes();
 
 // Launch helpers (cooperative launch so every CTA is co-resident).
-cudaError_t launch_ag_gemm(const AgParams& p, int grid, cudaStream_t s);
+int ag_max_pairs();  // clusters of 2 AG-GEMM CTAs that fit at once (0 on error)
+cudaError_t launch_ag_gemm(const AgParams& p, int pairs, cudaStream_t s);
 int rs_max_pairs();  // clusters of 2 GEMM-RS CTAs that fit at once (0 on error)
 cudaError_t launch_gemm_rs(const RsParams& p, int pairs, cudaStream_t s);
 cudaError_t launch_ring_allreduce(const RingParams& p, int sms, cudaStream_t s);

@@ -102,7 +102,7 @@ def test_flag_geometry(api):
     assert api.alltoall_num_flags(8, 65536) == 8 * 8 * 16
     assert api.alltoall_num_flags(3, 48) == 9
     assert api.alltoall_num_flags(3, 40) == -1
-    F, T = 2048, 64 * 16
+    F, T = 2048, 32 * 16  # 256x256 pair tiles
     assert api.ag_trace_words(8, 1024, 4096, 4096) == 2 * F + 2 * T + api.TRACE_MAX_CTAS
 
 

@@ -162,7 +162,7 @@ def test_fewer_ctas_than_sms(api):
 
 def _trace_views(api, prob, trace, grid):
     F = api.ag_num_flags(prob.R, prob.M_r, prob.K)
-    T = ((prob.M + 127) // 128) * ((prob.N + 255) // 256)
+    T = ((prob.M + 255) // 256) * ((prob.N + 255) // 256)  # 256x256 pair tiles
     t = trace.cpu().numpy().view(np.uint64)
     return dict(publish=t[:F], consume=t[F:2 * F], tile=t[2 * F:2 * F + T],
                 tile_start=t[2 * F + T:2 * F + 2 * T], cta_start=t[2 * F + 2 * T:2 * F + 2 * T + grid],
@@ -184,14 +184,15 @@ def test_trace_publish_before_consume_and_swizzle_order(api):
     # every tile published, and no consumer acquired a tile before its publish
     assert np.all(v["publish"] > 0) and np.all(v["consume"] != np.uint64(2 ** 64 - 1))
     assert np.all(v["publish"] <= v["consume"])
-    # each CTA visited its tiles in the oracle's swizzled order
-    T_M, T_N = prob.M // 128, (N + 255) // 256
-    cta = (v["tile"] >> np.uint64(32)).astype(np.int64)
+    # each consumer (a CTA pair) visited its 256x256 tiles in the oracle's
+    # swizzled order
+    T_M, T_N, pairs = prob.M // 256, (N + 255) // 256, grid // 2
+    pair = (v["tile"] >> np.uint64(32)).astype(np.int64)
     pos = (v["tile"] & np.uint64(0xFFFFFFFF)).astype(np.int64)
-    for c in range(grid):
-        mine = np.nonzero(cta == c)[0]
+    for c in range(pairs):
+        mine = np.nonzero(pair == c)[0]
         got = mine[np.argsort(pos[mine])]
-        assert list(got) == list(oracle.consumer_order(T_M, T_N, R, grid, c)), c
+        assert list(got) == list(oracle.consumer_order(T_M, T_N, R, pairs, c)), c
     G_ref, C_ref = prob.oracle_full()
     assert_gemm_close(host_bits(prob.C), C_ref)
 
