@@ -231,9 +231,11 @@ def run_reference(args, rank, world):
 # ------------------------------------------------------------------ our arm
 
 class TpLayer:
-    """Device-resident tp_layer workload and its two signal objects."""
+    """The tp_layer workload on the device: `sets` copies of every input and
+    output buffer (the end-to-end leg double-buffers them) and one signal
+    object per kernel, shared by the sets since its launches are serial."""
 
-    def __init__(self, api, torch, seed=0):
+    def __init__(self, api, torch, seed=0, sets=1):
         from overlap_producer_warps_gb300 import inputs
         self.api, self.torch = api, torch
         self.ag_cfg, self.rs_cfg = inputs.CONFIGS["ag_tp"], inputs.CONFIGS["rs_tp"]
@@ -241,28 +243,32 @@ class TpLayer:
         self.rs_d = inputs.rs_inputs(self.rs_cfg, seed=seed)
         a, r = self.ag_d, self.rs_d
         dev = torch.device("cuda")
-        self.ag_heap = torch.from_numpy(a["heap"]).to(dev)
-        self.B = torch.from_numpy(a["B"].view(np.int16)).to(dev).view(torch.bfloat16)
         M = a["R"] * a["M_r"]
-        self.G = torch.empty((M, a["K"]), dtype=torch.bfloat16, device=dev)
-        self.C = torch.empty((M, a["N"]), dtype=torch.bfloat16, device=dev)
-        self.rs_heap = torch.from_numpy(r["heap"]).to(dev)
+        self.bufs = []
+        for _ in range(sets):
+            self.bufs.append({
+                "ag_heap": torch.from_numpy(a["heap"]).to(dev),
+                "B": torch.from_numpy(a["B"].view(np.int16)).to(dev).view(torch.bfloat16),
+                "G": torch.empty((M, a["K"]), dtype=torch.bfloat16, device=dev),
+                "C": torch.empty((M, a["N"]), dtype=torch.bfloat16, device=dev),
+                "rs_heap": torch.from_numpy(r["heap"]).to(dev),
+            })
         self.sig_ag = api.Signal(api.ag_num_flags(a["R"], a["M_r"], a["K"]))
         self.sig_rs = api.Signal(api.rs_num_flags(r["R"], r["M"], r["N"]))
         self.flops_ag = flops_ag(self.ag_cfg)
         self.flops_rs = flops_rs(self.rs_cfg)
 
-    def ag(self, stream=None):
-        a = self.ag_d
-        self.api.ag_gemm(self.ag_heap, a["rank_off"], a["a_off"], a["M_r"], a["N"], a["K"],
-                         self.B, self.G, self.C, self.sig_ag, self.sig_ag.next_epoch(), None,
+    def ag(self, stream=None, b=0):
+        a, d = self.ag_d, self.bufs[b]
+        self.api.ag_gemm(d["ag_heap"], a["rank_off"], a["a_off"], a["M_r"], a["N"], a["K"],
+                         d["B"], d["G"], d["C"], self.sig_ag, self.sig_ag.next_epoch(), None,
                          stream)
 
-    def rs(self, stream=None):
+    def rs(self, stream=None, b=0):
         r = self.rs_d
-        self.api.gemm_rs(self.rs_heap, r["rank_off"], r["a_off"], r["b_off"], r["out_off"],
-                         r["M"], r["N"], r["K_r"], self.sig_rs, self.sig_rs.next_epoch(), None,
-                         stream)
+        self.api.gemm_rs(self.bufs[b]["rs_heap"], r["rank_off"], r["a_off"], r["b_off"],
+                         r["out_off"], r["M"], r["N"], r["K_r"], self.sig_rs,
+                         self.sig_rs.next_epoch(), None, stream)
 
     def check(self):
         for s in (self.sig_ag, self.sig_rs):
@@ -458,6 +464,91 @@ def per_config_results(api, torch, peak_tflops, reps=5):
     return out
 
 
+def e2e_results(torch, w, args, dist, world, flops_step):
+    """The step through the public API with its inputs and results in pinned
+    host memory.  Every step copies its inputs host -> device, runs AG-GEMM
+    and GEMM-RS, and reads C and every rank's output block back.  The steps
+    are pipelined over two device buffer sets and three streams: step i+1's
+    inputs go in and step i-1's results come out while step i computes.
+    The timed region runs from before step 0's first input copy to after the
+    last step's last result copy."""
+    a, r = w.ag_d, w.rs_d
+    h_ag = torch.from_numpy(a["heap"]).pin_memory()
+    h_B = torch.from_numpy(a["B"].view(np.int16)).pin_memory()
+    h_rs = torch.from_numpy(r["heap"]).pin_memory()
+    rs_in = []  # (offset, nbytes) of every A_r and B_r region
+    for rr in range(r["R"]):
+        o = int(r["rank_off"][rr])
+        rs_in.append((o + r["a_off"], r["M"] * r["K_r"] * 2))
+        rs_in.append((o + r["b_off"], r["K_r"] * r["N"] * 2))
+    Mb = r["M"] // r["R"]
+    nsets = len(w.bufs)
+    h_C = [torch.empty(w.bufs[0]["C"].shape, dtype=torch.bfloat16).pin_memory()
+           for _ in range(nsets)]
+    h_out = [torch.empty((r["R"], Mb * r["N"] * 2), dtype=torch.uint8).pin_memory()
+             for _ in range(nsets)]
+    h2d = h_ag.numel() + h_B.numel() * 2 + sum(n for _, n in rs_in)
+    d2h = h_C[0].numel() * 2 + h_out[0].numel()
+    stream, s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event(enable_timing=False)
+    in_done = [ev() for _ in range(nsets)]
+    comp_done = [ev() for _ in range(nsets)]
+    out_done = [ev() for _ in range(nsets)]
+    used = [False] * nsets
+
+    def e2e_step(i):
+        b = i % nsets
+        d = w.bufs[b]
+        with torch.cuda.stream(s_in):
+            if used[b]:
+                s_in.wait_event(comp_done[b])  # step i-2 has finished reading set b
+            d["ag_heap"].copy_(h_ag, non_blocking=True)
+            d["B"].view(torch.int16).copy_(h_B, non_blocking=True)
+            for o, n in rs_in:
+                d["rs_heap"][o:o + n].copy_(h_rs[o:o + n], non_blocking=True)
+            in_done[b].record(s_in)
+        stream.wait_event(in_done[b])
+        if used[b]:
+            stream.wait_event(out_done[b])  # step i-2's results are on the host
+        w.ag(stream, b)
+        w.rs(stream, b)
+        comp_done[b].record(stream)
+        used[b] = True
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[b])
+            h_C[b].copy_(d["C"], non_blocking=True)
+            for j in range(r["R"]):
+                o = int(r["rank_off"][j]) + r["out_off"]
+                h_out[b][j].copy_(d["rs_heap"][o:o + Mb * r["N"] * 2], non_blocking=True)
+            out_done[b].record(s_out)
+
+    def run(n, e0=None, e1=None):
+        if e0 is not None:
+            e0.record(stream)
+            s_in.wait_event(e0)
+        for i in range(n):
+            e2e_step(i)
+        for b in range(nsets):
+            if used[b]:
+                stream.wait_event(out_done[b])
+        if e1 is not None:
+            e1.record(stream)
+
+    run(max(1, min(args.warmup, 3)))
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    run(args.steps, e0, e1)
+    torch.cuda.synchronize()
+    w.check()
+    t_e2e = reduce_max(e0.elapsed_time(e1) / args.steps, dist, "cuda")
+    return {"value": whole_job_tflops(world, flops_step, t_e2e), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": t_e2e, "pipelined": f"{nsets} buffer sets, copy-in / compute / copy-out streams"}
+
+
 def run_ours(args, rank, world, dist):
     import torch
     from overlap_producer_warps_gb300 import api
@@ -470,7 +561,7 @@ def run_ours(args, rank, world, dist):
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
 
-    w = TpLayer(api, torch)
+    w = TpLayer(api, torch, sets=2)
     stream = torch.cuda.current_stream()
 
     def step(evs=None):
@@ -511,51 +602,7 @@ def run_ours(args, rank, world, dist):
     value = whole_job_tflops(world, flops_step, t_step)
 
     # ---- end to end through the public API with host buffers
-    a, r = w.ag_d, w.rs_d
-    h_ag = torch.from_numpy(a["heap"]).pin_memory()
-    h_B = torch.from_numpy(a["B"].view(np.int16)).pin_memory()
-    h_rs = torch.from_numpy(r["heap"]).pin_memory()
-    rs_in = []  # (offset, nbytes) of every A_r and B_r region
-    for rr in range(r["R"]):
-        o = int(r["rank_off"][rr])
-        rs_in.append((o + r["a_off"], r["M"] * r["K_r"] * 2))
-        rs_in.append((o + r["b_off"], r["K_r"] * r["N"] * 2))
-    h_C = torch.empty(w.C.shape, dtype=torch.bfloat16).pin_memory()
-    Mb = r["M"] // r["R"]
-    h_out = torch.empty((r["R"], Mb * r["N"] * 2), dtype=torch.uint8).pin_memory()
-    B_u16 = w.B.view(torch.int16)
-    h2d = h_ag.numel() + h_B.numel() * 2 + sum(n for _, n in rs_in)
-    d2h = h_C.numel() * 2 + h_out.numel()
-
-    def e2e_step():
-        w.ag_heap.copy_(h_ag, non_blocking=True)
-        B_u16.copy_(h_B, non_blocking=True)
-        for o, n in rs_in:
-            w.rs_heap[o:o + n].copy_(h_rs[o:o + n], non_blocking=True)
-        w.ag()
-        w.rs()
-        h_C.copy_(w.C, non_blocking=True)
-        for j in range(r["R"]):
-            o = int(r["rank_off"][j]) + r["out_off"]
-            h_out[j].copy_(w.rs_heap[o:o + Mb * r["N"] * 2], non_blocking=True)
-
-    for _ in range(max(1, min(args.warmup, 3))):
-        e2e_step()
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    w.check()
-    t_e2e = reduce_max(e0.elapsed_time(e1) / args.steps, dist, "cuda")
-    e2e = {"value": whole_job_tflops(world, flops_step, t_e2e), "unit": UNIT,
-           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-           "ms_per_step": t_e2e}
+    e2e = e2e_results(torch, w, args, dist, world, flops_step)
 
     # ---- roofline of the dominant kernel (device time share)
     dom = "gemm_rs" if rs_ms >= ag_ms else "ag_gemm"

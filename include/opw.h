@@ -246,6 +246,12 @@ int64_t opw_ag_trace_words(int32_t R, int64_t M_r, int64_t N, int64_t K);
  * cta_group::2 MMAs with TMEM accumulators.  After the launch every flag slot
  * holds `epoch` and G is bit-identical to the concatenation.
  *
+ * The kernel is launched cooperatively (every CTA resident at once, which the
+ * flag waits between CTAs need).  ncu cannot profile a cooperative clustered
+ * launch: with the environment variable OPW_AG_LAUNCH_NONCOOPERATIVE set when
+ * the library is first used, the cooperative attribute is left out (the grid
+ * is still sized to be resident) so the kernel can be captured.
+ *
  * Shapes: M_r, K multiples of 64 (flag tile 64) or 128; N a multiple of 8;
  * R*M_r, N, K <= 2^31.  Alignment: heap_dev, B_dev, G_dev, C_dev, a_off and
  * rank_off[] multiples of 16 bytes.  G and C must not overlap any A_r or B.

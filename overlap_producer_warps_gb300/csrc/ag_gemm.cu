@@ -33,6 +33,8 @@
 // signal object's status word, drains its own in-flight copies and MMAs,
 // frees TMEM and returns.  Cluster barriers bracket the kernel, so neither CTA
 // of a pair leaves while the other may still use its shared memory or TMEM.
+#include <cstdlib>
+
 #include "opw_device.cuh"
 #include "opw_kernels.h"
 
@@ -749,11 +751,15 @@ cudaLaunchConfig_t pair_config(unsigned pairs, cudaStream_t s, cudaLaunchAttribu
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     // Consumers wait on flags that other CTAs' producers publish: every CTA
-    // must be resident at once.
+    // must be resident at once.  The cooperative attribute guarantees it.
+    // ncu cannot launch a kernel that is both cooperative and clustered, so
+    // OPW_AG_LAUNCH_NONCOOPERATIVE=1 leaves the attribute out for profiling;
+    // the grid, sized by the cluster occupancy query, still fits the GPU.
+    static const bool coop = std::getenv("OPW_AG_LAUNCH_NONCOOPERATIVE") == nullptr;
     attr[1].id = cudaLaunchAttributeCooperative;
     attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = coop ? 2 : 1;
     return cfg;
 }
 
