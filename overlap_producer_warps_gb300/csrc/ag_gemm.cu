@@ -13,7 +13,7 @@
 // receives its 128 accumulator rows in its own TMEM.  8 warps per CTA:
 //   warp 0     loader (both CTAs): takes tiles from the on-chip tile queue and
 //              TMA-loads this CTA's half of their A k-blocks (from the gathered
-//              buffer G) and B k-blocks into a 6-stage ring; the bytes of both
+//              buffer G) and B k-blocks into a 5-stage ring; the bytes of both
 //              halves complete on the even CTA's `full` barrier.
 //   warp 1     MMA (even CTA only): one thread issues the pair's tcgen05.mma
 //              (bf16 x bf16 -> fp32) into a double-buffered TMEM accumulator
@@ -41,7 +41,8 @@
 namespace opw {
 namespace {
 
-constexpr int AG_STAGES = 6;
+constexpr int AG_STAGES = 5;
+constexpr int GATHER_BUFS = 4;  // producer staging buffers (a power of 2)
 constexpr int HALF_N = BN / 2;                  // B columns held by each CTA
 constexpr int B_HALF_BYTES = BK * HALF_N * 2;   // 16 KiB: 2 chunks of 64 columns
 constexpr uint32_t PAIR_TX_BYTES = 2u * (A_STAGE_BYTES + B_HALF_BYTES);
@@ -51,7 +52,7 @@ struct AgCtrl {
     uint64_t empty[AG_STAGES];  // each CTA: the pair MMA is done with its stage
     uint64_t tmem_full[2];      // each CTA: an accumulator is complete in its TMEM
     uint64_t tmem_empty[2];     // even CTA: both CTAs' epilogues have read it
-    uint64_t gfull[2];
+    uint64_t gfull[GATHER_BUFS];
     uint64_t tq_full[TILE_Q];   // each CTA: a tile id is in its queue slot
     uint64_t tq_empty[TILE_Q];  // even CTA: every reader of the slot, in both CTAs, is done
     uint64_t need_next;         // even CTA, loader -> scheduler: claim the next tile now
@@ -65,7 +66,7 @@ constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + AG_STAGES * A_STAGE_BYTES;
 constexpr int OFF_EPI = OFF_B + AG_STAGES * B_HALF_BYTES;
 constexpr int OFF_GATHER = OFF_EPI + 4 * EPI_WARP_BYTES;
-constexpr int OFF_CTRL = OFF_GATHER + 2 * GATHER_BUF_BYTES;
+constexpr int OFF_CTRL = OFF_GATHER + GATHER_BUFS * GATHER_BUF_BYTES;
 constexpr int SMEM_ALLOC = OFF_CTRL + static_cast<int>(sizeof(AgCtrl)) + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget (227 KiB per CTA)");
 static_assert(OFF_B % 1024 == 0 && OFF_EPI % 1024 == 0 && OFF_GATHER % 1024 == 0,
@@ -544,7 +545,7 @@ __device__ void run_gather(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
     const int n_mine = c < n_items ? (n_items - c + G - 1) / G : 0;
     uint8_t* buf0 = smem + OFF_GATHER;
     int ordered_upto = 0;  // rank positions whose predecessors are known complete
-    uint32_t seq = 0;      // sub-box sequence number: buffer seq & 1, phase (seq >> 1) & 1
+    uint32_t seq = 0;      // sub-box sequence number across this warp's flag tiles
     bool ok = true;
 
     for (int it = 0; it < n_mine && ok; ++it) {
@@ -594,38 +595,48 @@ __device__ void run_gather(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
             ordered_upto = ip;
         }
 
-        // Copy the flag tile 32 rows at a time through two staging buffers:
-        // TMA load A_r rows -> shared, then TMA store shared -> G.
+        // Copy the flag tile 32 rows at a time through the staging buffers:
+        // TMA loads of A_r rows -> shared (up to GATHER_BUFS in flight), then
+        // a TMA store shared -> G as each one lands.  Sub-box number `sq`
+        // uses buffer sq % GATHER_BUFS for the (sq / GATHER_BUFS)-th time.
         const int x = kt * p.ft;
         const int y_src = mt * p.ft;
         const int y_dst = r * p.M_r + mt * p.ft;
         auto issue_load = [&](uint32_t sq, int sub) {
             if (lane == 0) {
-                bulk_wait_read<0>();  // earlier stores are done reading the staging buffer
-                uint64_t* fb = &ctrl->gfull[sq & 1u];
+                bulk_wait_read<0>();  // earlier stores are done reading the staging buffers
+                uint64_t* fb = &ctrl->gfull[sq % GATHER_BUFS];
                 mbar_arrive_expect_tx(fb, sub_bytes);
-                tma_load_2d(buf0 + (sq & 1u) * GATHER_BUF_BYTES, &p.shard[r], fb, x,
+                tma_load_2d(buf0 + (sq % GATHER_BUFS) * GATHER_BUF_BYTES, &p.shard[r], fb, x,
                             y_src + sub * GATHER_SUB_ROWS);
             }
             __syncwarp();
         };
-        issue_load(seq, 0);
+        const int ahead = subs < GATHER_BUFS ? subs : GATHER_BUFS;
+        for (int sub = 0; sub < ahead; ++sub) issue_load(seq + sub, sub);
+        int issued = ahead;
         for (int sub = 0; sub < subs; ++sub) {
-            if (sub + 1 < subs) issue_load(seq + 1, sub + 1);
-            if (!wait_bar(&ctrl->gfull[seq & 1u], (seq >> 1) & 1u, ec, SITE_GATHER_LOAD)) {
-                // both outstanding loads must land before the CTA may exit
-                drain_bar(&ctrl->gfull[seq & 1u], (seq >> 1) & 1u, ec);
-                if (sub + 1 < subs) drain_bar(&ctrl->gfull[(seq + 1) & 1u], ((seq + 1) >> 1) & 1u, ec);
+            if (!wait_bar(&ctrl->gfull[seq % GATHER_BUFS], (seq / GATHER_BUFS) & 1u, ec,
+                          SITE_GATHER_LOAD)) {
+                // every outstanding load must land before the CTA may exit
+                for (int k = sub; k < issued; ++k) {
+                    const uint32_t sq = seq + (k - sub);
+                    drain_bar(&ctrl->gfull[sq % GATHER_BUFS], (sq / GATHER_BUFS) & 1u, ec);
+                }
                 ok = false;
                 break;
             }
             if (lane == 0) {
-                tma_store_2d(&p.g_store, buf0 + (seq & 1u) * GATHER_BUF_BYTES, x,
+                tma_store_2d(&p.g_store, buf0 + (seq % GATHER_BUFS) * GATHER_BUF_BYTES, x,
                              y_dst + sub * GATHER_SUB_ROWS);
                 bulk_commit();
             }
             __syncwarp();
             ++seq;
+            if (issued < subs) {
+                issue_load(seq + (issued - sub - 1), issued);
+                ++issued;
+            }
         }
         if (!ok) break;
 
@@ -678,8 +689,8 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctrl->tmem_full[i], 1);
             mbar_init(&ctrl->tmem_empty[i], 2 * 4);  // 4 epilogue warps in each CTA
-            mbar_init(&ctrl->gfull[i], 1);
         }
+        for (int i = 0; i < GATHER_BUFS; ++i) mbar_init(&ctrl->gfull[i], 1);
         for (int i = 0; i < TILE_Q; ++i) {
             mbar_init(&ctrl->tq_full[i], 1);
             mbar_init(&ctrl->tq_empty[i], TQ_READERS);

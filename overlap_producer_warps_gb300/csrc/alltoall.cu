@@ -4,7 +4,7 @@
 // and waits until each peer's slice has arrived in its own buffer).
 //
 // On one GPU every rank's send and receive buffers are slices of the heap.
-// A slice of B bytes is cut into 4 KiB pieces; a warp copies one piece
+// A slice of B bytes is cut into 8 KiB pieces; a warp copies one piece
 // (16-byte loads and stores that bypass L1) and, for a peer, releases the
 // flag of (receiver j, sender r, piece) with the epoch.  The receiving side
 // then acquires every incoming flag (>= epoch, bounded wait): the
@@ -19,8 +19,8 @@ namespace opw {
 namespace {
 
 constexpr int A2A_THREADS = 256;
-constexpr int A2A_PIECE = 4096;                 // bytes per warp action
-constexpr int A2A_VEC = A2A_PIECE / 16 / 32;    // uint4 per lane (8)
+constexpr int A2A_PIECE = 8192;                 // bytes per warp action
+constexpr int A2A_VEC = A2A_PIECE / 16 / 32;    // uint4 per lane (16)
 
 struct A2aParams {
     char* heap;
