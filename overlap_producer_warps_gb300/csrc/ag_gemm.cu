@@ -475,8 +475,8 @@ __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uin
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
     uint8_t* buf = smem + OFF_EPI + quarter * EPI_WARP_BYTES;
     const uint32_t row_addr = smem_u32(buf) + lane * 128u;
-    uint32_t empty_caddr[2];
-    for (int a = 0; a < 2; ++a) empty_caddr[a] = mapa_shared(smem_u32(&ctrl->tmem_empty[a]), 0);
+    // the even CTA's tmem_empty[0], [1] (adjacent 8-byte barriers)
+    const uint32_t empty_caddr0 = mapa_shared(smem_u32(&ctrl->tmem_empty[0]), 0);
     uint32_t acc = 0, aphase = 0, tq = 0, tqphase = 0;
     while (true) {
         const int q = pop_tile(ctrl, ec, tq, tqphase);
@@ -499,7 +499,7 @@ __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uin
                 // accumulator fully read: the MMA may reuse it
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(empty_caddr[acc]);
+                if (lane == 0) mbar_arrive_cluster(empty_caddr0 + 8u * acc);
             }
             uint32_t w[32];
 #pragma unroll

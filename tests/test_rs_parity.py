@@ -81,6 +81,31 @@ def test_pair_counts(api, num_ctas):
     _check_all(api, prob)
 
 
+def test_output_independent_of_pair_count(api):
+    """Each pair reduces its tiles' partials in rank order in fp32, whatever
+    the grid: 64 pair tiles on 8, 12, 13 and 21 pairs (0, 4, 12 and 1 tiles in
+    the last partial wave) must give bit-identical outputs."""
+    R, M, K_r, N = 4, 4096, 192, 1024
+    d = inputs.rs_inputs(_cfg(R, M, K_r, N), seed=45)
+    prob = RsProblem(d)
+    F = api.rs_num_flags(R, M, N)
+    outs = []
+    for num_ctas in (16, 24, 26, 42):
+        sig = api.Signal(F)
+        for _ in range(2):
+            e = sig.next_epoch()
+            prob.run(api, sig, e, api.make_opts(num_ctas=num_ctas))
+            st = sig.status()
+            assert st[0] == api.OK, (num_ctas, st)
+            assert np.all(sig.flags().cpu().numpy() == e)
+        outs.append(np.concatenate([prob.out_bits(j) for j in range(R)]))
+        sig.close()
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    rows = sample_rows(prob.M, 128, 1, seed=3)
+    _check_all(api, prob, rows)
+
+
 def test_deterministic_and_epochs(api):
     R, M, K_r, N = 4, 512, 256, 512
     d = inputs.rs_inputs(_cfg(R, M, K_r, N), seed=31)
