@@ -138,6 +138,13 @@ typedef struct {
 #define OPW_SYNC_SERIAL  1   /* consumers wait until EVERY tile is published
                                 (the "test with barrier sync first" debug mode
                                 of "Triton-distributed Semantics", Best Practices 8) */
+#define OPW_SYNC_CHECKED 2   /* as OVERLAP, but every publish is an atomic exchange
+                                that must find epoch-1 in the slot (with
+                                OPW_SIGNAL_ROW_ADD: a fetch-add that must find a
+                                count of this epoch's window), so each slot is
+                                published exactly once per epoch; otherwise the
+                                launch stops with OPW_ERR_FLAG_PROTOCOL (rank, slot).
+                                AG-GEMM and GEMM-RS. */
 
 #define OPW_SCHED_READY   0  /* dynamic (default): CTAs claim output tiles from a
                                 device counter in the order their rows are

@@ -26,7 +26,7 @@ ERR_TIMEOUT = 6
 ERR_FLAG_PROTOCOL = 7
 ERR_NOT_READY = 8
 
-SYNC_OVERLAP, SYNC_SERIAL = 0, 1
+SYNC_OVERLAP, SYNC_SERIAL, SYNC_CHECKED = 0, 1, 2
 SCHED_READY, SCHED_SWIZZLE = 0, 1
 ROLE_FUSED, ROLE_PRODUCER, ROLE_CONSUMER = 0, 1, 2
 FAULT_NONE, FAULT_DROP_TILE, FAULT_STALE_EPOCH = 0, 1, 2

@@ -652,13 +652,29 @@ __device__ void run_gather(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
             // the publish time is read before the release, so no consumer can
             // observe the flag earlier than the recorded time
             const uint64_t t_pub = p.trace != nullptr ? globaltimer() : 0;
+            const bool checked = p.sync_mode == OPW_SYNC_CHECKED;
             if (p.signal_mode == OPW_SIGNAL_ROW_ADD) {
                 // batched signal: one counter per flag row, +1 per k-tile
-                if (!skip && v == static_cast<int64_t>(p.epoch))
-                    red_release_add(reinterpret_cast<unsigned long long*>(p.flags) + r * p.T_mr + mt,
-                                    1ull);
+                if (!skip && v == static_cast<int64_t>(p.epoch)) {
+                    unsigned long long* ctr =
+                        reinterpret_cast<unsigned long long*>(p.flags) + r * p.T_mr + mt;
+                    if (checked) {
+                        // this epoch's adds take the counter from (e-1)*T_k to e*T_k
+                        const uint64_t old = atom_add_release(ctr, 1ull);
+                        const uint64_t lo = (p.epoch - 1) * static_cast<uint64_t>(p.T_k);
+                        if (old < lo || old >= lo + static_cast<uint64_t>(p.T_k))
+                            raise_error(ec, OPW_ERR_FLAG_PROTOCOL, r, r * p.T_mr + mt);
+                    } else {
+                        red_release_add(ctr, 1ull);
+                    }
+                }
             } else if (!skip) {
-                st_release(p.flags + slot, v);
+                if (checked) {
+                    if (atom_exch_release(p.flags + slot, v) != static_cast<int64_t>(p.epoch) - 1)
+                        raise_error(ec, OPW_ERR_FLAG_PROTOCOL, r, slot);
+                } else {
+                    st_release(p.flags + slot, v);
+                }
             }
             red_release_add(p.counters + CTR_RANK_DONE + r, 1ull);
             if (p.trace != nullptr) p.trace[slot] = t_pub;

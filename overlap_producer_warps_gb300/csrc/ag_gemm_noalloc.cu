@@ -120,7 +120,9 @@ extern "C" opw_status opw_ag_gemm_noalloc(const opw_symm* symm, size_t a_off, in
     std::memset(&o, 0, sizeof o);
     if (opts_in != nullptr) o = *opts_in;
     if (o.role != OPW_ROLE_FUSED) return OPW_ERR_INVALID_ARG;  // no epochs persist between calls
-    if (o.sync_mode != OPW_SYNC_OVERLAP && o.sync_mode != OPW_SYNC_SERIAL) return OPW_ERR_INVALID_ARG;
+    if (o.sync_mode != OPW_SYNC_OVERLAP && o.sync_mode != OPW_SYNC_SERIAL &&
+        o.sync_mode != OPW_SYNC_CHECKED)
+        return OPW_ERR_INVALID_ARG;
     if (o.schedule != OPW_SCHED_SWIZZLE && o.schedule != OPW_SCHED_READY) return OPW_ERR_INVALID_ARG;
     if (o.fault_kind < OPW_FAULT_NONE || o.fault_kind > OPW_FAULT_STALE_EPOCH) return OPW_ERR_INVALID_ARG;
     if (o.num_ctas < 0) return OPW_ERR_INVALID_ARG;

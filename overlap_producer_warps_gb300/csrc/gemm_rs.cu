@@ -277,7 +277,13 @@ __device__ void rs_reduce(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32
                 if (ntile < p.T_fn) {
                     const int slot = (j * p.T_fm + mt) * p.T_fn + ntile;
                     const uint64_t t_pub = p.trace != nullptr ? globaltimer() : 0;
-                    st_release(p.flags + slot, static_cast<int64_t>(p.epoch));
+                    if (p.checked) {
+                        if (atom_exch_release(p.flags + slot, static_cast<int64_t>(p.epoch)) !=
+                            static_cast<int64_t>(p.epoch) - 1)
+                            raise_error(ec, OPW_ERR_FLAG_PROTOCOL, j, slot);
+                    } else {
+                        st_release(p.flags + slot, static_cast<int64_t>(p.epoch));
+                    }
                     if (p.trace != nullptr) p.trace[slot] = t_pub;
                 }
             }

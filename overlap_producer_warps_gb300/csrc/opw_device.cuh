@@ -180,6 +180,20 @@ __device__ __forceinline__ void st_release(int64_t* p, int64_t v)
     asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+__device__ __forceinline__ int64_t atom_exch_release(int64_t* p, int64_t v)
+{
+    int64_t old;
+    asm volatile("atom.exch.release.gpu.global.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint64_t atom_add_release(unsigned long long* p, unsigned long long v)
+{
+    uint64_t old;
+    asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void red_release_add(unsigned long long* p, unsigned long long v)
 {
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");

@@ -270,7 +270,9 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
         return OPW_ERR_INVALID_ARG;
     opw_opts tmp;
     const opw_opts& o = opts_or_default(opts_in, tmp);
-    if (o.sync_mode != OPW_SYNC_OVERLAP && o.sync_mode != OPW_SYNC_SERIAL) return OPW_ERR_INVALID_ARG;
+    if (o.sync_mode != OPW_SYNC_OVERLAP && o.sync_mode != OPW_SYNC_SERIAL &&
+        o.sync_mode != OPW_SYNC_CHECKED)
+        return OPW_ERR_INVALID_ARG;
     if (o.schedule != OPW_SCHED_SWIZZLE && o.schedule != OPW_SCHED_READY) return OPW_ERR_INVALID_ARG;
     if (o.role < OPW_ROLE_FUSED || o.role > OPW_ROLE_CONSUMER) return OPW_ERR_INVALID_ARG;
     if (o.fault_kind < OPW_FAULT_NONE || o.fault_kind > OPW_FAULT_STALE_EPOCH) return OPW_ERR_INVALID_ARG;
@@ -401,9 +403,9 @@ opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t 
     if (sig == nullptr) return OPW_ERR_INVALID_ARG;
     opw_opts tmp;
     const opw_opts& o = opts_or_default(opts_in, tmp);
-    if (o.sync_mode != 0 || o.schedule != 0 || o.role != 0 || o.publish_perm != nullptr ||
-        o.delay_ns != nullptr || o.fault_kind != 0 || o.num_ctas < 0 || o.signal_mode != 0 ||
-        o.reserved != 0)
+    if ((o.sync_mode != OPW_SYNC_OVERLAP && o.sync_mode != OPW_SYNC_CHECKED) || o.schedule != 0 ||
+        o.role != 0 || o.publish_perm != nullptr || o.delay_ns != nullptr || o.fault_kind != 0 ||
+        o.num_ctas < 0 || o.signal_mode != 0 || o.reserved != 0)
         return OPW_ERR_INVALID_ARG;
     const int R = symm->R;
     if (M <= 0 || N <= 0 || K_r <= 0 || M % (128 * R) != 0 || N % 8 != 0 || K_r % 8 != 0)
@@ -455,6 +457,7 @@ opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t 
     p.T_N = static_cast<int32_t>((N + BN - 1) / BN);
     p.T_fm = static_cast<int32_t>(Mb / 128);
     p.T_fn = static_cast<int32_t>((N + 127) / 128);
+    p.checked = o.sync_mode == OPW_SYNC_CHECKED;
     if (launch_gemm_rs(p, pairs, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return OPW_ERR_CUDA;
     sig->epoch_last = epoch;

@@ -85,6 +85,7 @@ struct RsParams {
     int32_t R, M, N, K_r, Mb;
     int32_t T_M, T_N;         // 256 x 256 pair tiles along M, along N
     int32_t T_fm, T_fn;       // 128x128 flag tiles per rank block along M, along N
+    int32_t checked;          // OPW_SYNC_CHECKED: publish by exchange, expect epoch-1
 };
 
 struct RingParams {

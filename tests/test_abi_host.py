@@ -74,6 +74,17 @@ int main(void) {
     assert symm == [ctypes.sizeof(S)] + [getattr(S, f).offset for f, _ in S._fields_]
 
 
+def test_binding_constants_match_the_header(api):
+    """Every OPW_* enum value the binding uses equals the header's #define."""
+    defs = dict(re.findall(r"^#define OPW_(\w+)\s+(-?\d+)", open(HEADER).read(), re.M))
+    names = [n for n in dir(api) if n.isupper() and not n.startswith("_") and n in defs]
+    for n in ("OK", "ERR_FLAG_PROTOCOL", "SYNC_CHECKED", "SCHED_SWIZZLE", "ROLE_CONSUMER",
+              "FAULT_STALE_EPOCH", "SIGNAL_ROW_ADD", "MAX_RANKS", "TRACE_MAX_CTAS"):
+        assert n in names, n
+    for n in names:
+        assert getattr(api, n) == int(defs[n]), n
+
+
 def test_status_strings(api):
     for code, name in [(0, "OK"), (1, "INVALID_ARG"), (2, "UNSUPPORTED_SHAPE"), (3, "MISALIGNED"),
                        (4, "BAD_EPOCH"), (5, "CUDA_ERROR"), (6, "TIMEOUT"), (7, "FLAG_PROTOCOL"),

@@ -88,3 +88,64 @@ def test_row_add_missing_increment_times_out(api):
                                                        signal_mode=api.SIGNAL_ROW_ADD))
     status, rank, where = sig.status()
     assert (status, rank, where) == (api.ERR_TIMEOUT, 2, 2)
+
+
+def _plant(sig, slot, value):
+    """Write `value` into one flag slot behind the kernels' back."""
+    flags = sig.flags()
+    flags[slot] = value
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("mode", ["set", "row_add"])
+def test_checked_publish_finds_the_previous_epoch(api, mode):
+    """OPW_SYNC_CHECKED publishes by exchange (SET) or fetch-add (ROW_ADD) and
+    requires the previous epoch's value; a planted value is reported as
+    FLAG_PROTOCOL with the producing rank and the slot, and the signal object
+    recovers after a reset."""
+    prob = _problem(seed=41)
+    row_add = mode == "row_add"
+    F = api.ag_num_row_counters(4, 128, 256) if row_add else api.ag_num_flags(4, 128, 256)
+    sm = api.SIGNAL_ROW_ADD if row_add else api.SIGNAL_TILE_SET
+    sig = api.Signal(F)
+
+    def opts():
+        return api.make_opts(sync_mode=api.SYNC_CHECKED, signal_mode=sm, timeout_ns=TIMEOUT_NS)
+
+    for _ in range(3):
+        prob.run(api, sig, sig.next_epoch(), opts())
+        assert sig.status()[0] == api.OK
+    _, C_ref = prob.oracle_full()
+    assert_gemm_close(host_bits(prob.C), C_ref)
+    e = sig.next_epoch()
+    # flag tiles are 128x128 here: 4 ranks x 1 row x 2 k-columns (T_k = 2)
+    if row_add:
+        slot, rank = 2, 2
+        _plant(sig, slot, e * 2 + 3)      # outside this epoch's window [(e-1)*2, e*2)
+    else:
+        slot, rank = 5, 2
+        _plant(sig, slot, e + 3)          # not e - 1
+    prob.run(api, sig, e, opts())
+    assert sig.status() == (api.ERR_FLAG_PROTOCOL, rank, slot)
+    sig.reset()
+    prob.run(api, sig, sig.next_epoch(), opts())
+    assert sig.status()[0] == api.OK
+
+
+def test_gemm_rs_checked_publish_finds_the_previous_epoch(api):
+    from tests.helpers import RsProblem
+    d = inputs.rs_inputs(dict(R=2, M=256, K_r=128, N=256, dist="normal", scale=0.5), seed=50)
+    prob = RsProblem(d)
+    F = api.rs_num_flags(2, 256, 256)          # 2 ranks x 1 x 2 output tiles
+    sig = api.Signal(F)
+    opts = api.make_opts(sync_mode=api.SYNC_CHECKED, timeout_ns=TIMEOUT_NS)
+    for _ in range(3):
+        prob.run(api, sig, sig.next_epoch(), opts)
+        assert sig.status()[0] == api.OK
+    e = sig.next_epoch()
+    _plant(sig, 3, e + 3)
+    prob.run(api, sig, e, opts)
+    assert sig.status() == (api.ERR_FLAG_PROTOCOL, 1, 3)  # slot 3 belongs to rank 1
+    sig.reset()
+    prob.run(api, sig, sig.next_epoch(), opts)
+    assert sig.status()[0] == api.OK
