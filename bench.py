@@ -559,7 +559,13 @@ def run_ours(args, rank, world, dist):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     peaks, peak_src = load_peaks()
-    peak = float(peaks["bf16_tflops"])
+    peak = float(peaks["bf16_tflops"])  # burst: a kernel timed alone
+    # The timed steps follow args.prewarm_s of load, where the 1.4 kW power
+    # cap holds the clocks down: compare them with the sustained figure.
+    sustained = args.prewarm_s >= 1.0 and "bf16_tflops_sustained" in peaks
+    step_peak = float(peaks["bf16_tflops_sustained"]) if sustained else peak
+    step_peak_name = ("bf16_tflops_sustained (cuBLAS back to back, under the power cap)"
+                      if sustained else "bf16_tflops (burst, cuBLAS)")
 
     w = TpLayer(api, torch, sets=2)
     stream = torch.cuda.current_stream()
@@ -576,6 +582,13 @@ def run_ours(args, rank, world, dist):
 
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
+    # An idle GPU needs seconds of load before its clocks settle: run the
+    # step, untimed, for args.prewarm_s before the W counted warm-up steps.
+    t_pre = time.perf_counter() + args.prewarm_s
+    while time.perf_counter() < t_pre:
+        for _ in range(10):
+            step()
+        torch.cuda.synchronize()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -609,9 +622,9 @@ def run_ours(args, rank, world, dist):
     dom_ms = rs_ms if dom == "gemm_rs" else ag_ms
     dom_flops = w.flops_rs if dom == "gemm_rs" else w.flops_ag
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS)",
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": step_peak,
+                "unit": "TFLOP/s", "frac": achieved / step_peak,
+                "peak_source": f"{peak_src} {step_peak_name}",
                 "traffic": kernel_traffic(dom),
                 "ms_per_launch": {"ag_gemm": ag_ms, "gemm_rs": rs_ms}}
 
@@ -621,8 +634,9 @@ def run_ours(args, rank, world, dist):
             "impl": "ours",
             "config": {"workload": WORKLOAD, "R": 8, "epochs": "fresh epoch per launch, no reset",
                        "l2": "inputs larger than L2 (656 MiB read per step vs 129 MB L2)",
+                       "prewarm_s": args.prewarm_s,
                        "parallelism": f"replicas x{world}"},
-            "pct_of_peak": value / world / peak,
+            "pct_of_peak": value / world / step_peak,
             "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks}
 
     if rank == 0 and world == 1 and not args.no_extra:
@@ -644,6 +658,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the per-configuration table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--prewarm-s", type=float, default=2.0,
+                    help="seconds of untimed steps before the warm-up steps (clock ramp)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
