@@ -18,10 +18,8 @@
 // kernels.
 #include <cuda.h>
 #include <cuda_runtime.h>
-#include <cudaTypedefs.h>
 
 #include <cstdint>
-#include <cstring>
 #include <mutex>
 
 #include "../../include/opw.h"
@@ -72,36 +70,6 @@ __global__ void noalloc_clear_kernel(int64_t* flags, int64_t n_flags, unsigned l
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-              uint32_t box_rows, CUtensorMapSwizzle sw)
-{
-    auto fn = encode_fn();
-    if (fn == nullptr) return false;
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {box_cols, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
@@ -111,111 +79,39 @@ extern "C" opw_status opw_ag_gemm_noalloc(const opw_symm* symm, size_t a_off, in
                                           void* stream)
 {
     // ---- arguments, all before any CUDA call
-    if (symm == nullptr || symm->heap_dev == nullptr || symm->rank_off == nullptr ||
-        symm->R < 1 || symm->R > OPW_MAX_RANKS || symm->reserved != 0)
-        return OPW_ERR_INVALID_ARG;
-    if (B_dev == nullptr || G_dev == nullptr || C_dev == nullptr || status_dev == nullptr)
-        return OPW_ERR_INVALID_ARG;
     opw_opts o;
-    std::memset(&o, 0, sizeof o);
+    opw_opts_default(&o);
     if (opts_in != nullptr) o = *opts_in;
+    if (status_dev == nullptr) return OPW_ERR_INVALID_ARG;
     if (o.role != OPW_ROLE_FUSED) return OPW_ERR_INVALID_ARG;  // no epochs persist between calls
-    if (o.sync_mode != OPW_SYNC_OVERLAP && o.sync_mode != OPW_SYNC_SERIAL &&
-        o.sync_mode != OPW_SYNC_CHECKED)
-        return OPW_ERR_INVALID_ARG;
-    if (o.schedule != OPW_SCHED_SWIZZLE && o.schedule != OPW_SCHED_READY) return OPW_ERR_INVALID_ARG;
-    if (o.fault_kind < OPW_FAULT_NONE || o.fault_kind > OPW_FAULT_STALE_EPOCH) return OPW_ERR_INVALID_ARG;
-    if (o.num_ctas < 0) return OPW_ERR_INVALID_ARG;
-    if ((o.signal_mode != OPW_SIGNAL_TILE_SET && o.signal_mode != OPW_SIGNAL_ROW_ADD) ||
-        o.reserved != 0)
-        return OPW_ERR_INVALID_ARG;
+    int64_t ft = 0;
+    const opw_status st_args = ag_check_args(symm, a_off, M_r, N, K, B_dev, G_dev, C_dev, o, &ft);
+    if (st_args != OPW_OK) return st_args;
     const int R = symm->R;
-    if (o.publish_perm != nullptr) {
-        bool seen[OPW_MAX_RANKS] = {};
-        for (int i = 0; i < R; ++i) {
-            const int r = o.publish_perm[i];
-            if (r < 0 || r >= R || seen[r]) return OPW_ERR_INVALID_ARG;
-            seen[r] = true;
-        }
-    }
-    const int64_t ft = opw_ag_flag_tile(M_r, K);
-    if (ft < 0 || N <= 0 || N % 8 != 0) return OPW_ERR_UNSUPPORTED_SHAPE;
-    const int64_t M = static_cast<int64_t>(R) * M_r;
-    if (M > (int64_t(1) << 31) || N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
-        return OPW_ERR_UNSUPPORTED_SHAPE;
-    const int64_t F = static_cast<int64_t>(R) * (M_r / ft) * (K / ft);
+    const bool row_add = o.signal_mode == OPW_SIGNAL_ROW_ADD;
+    const int64_t F = static_cast<int64_t>(R) * (M_r / ft) * (row_add ? 1 : K / ft);
     if (F > kMaxFlags) return OPW_ERR_UNSUPPORTED_SHAPE;  // beyond the fixed scratch
-    if (!aligned16(symm->heap_dev) || !aligned16(B_dev) || !aligned16(G_dev) || !aligned16(C_dev) ||
-        !aligned16(status_dev) || (a_off & 15u) != 0 ||
-        (o.trace_dev != nullptr && (reinterpret_cast<uintptr_t>(o.trace_dev) & 7u) != 0))
-        return OPW_ERR_MISALIGNED;
-    for (int r = 0; r < R; ++r) {
-        if (symm->rank_off[r] < 0) return OPW_ERR_INVALID_ARG;
-        if ((symm->rank_off[r] & 15) != 0) return OPW_ERR_MISALIGNED;
-    }
+    if ((reinterpret_cast<uintptr_t>(status_dev) & 15u) != 0) return OPW_ERR_MISALIGNED;
 
     // ---- set-up for this device (first call only), then the launches
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return OPW_ERR_CUDA;
     void* scratch = nullptr;
     if (scratch_for_device(dev, &scratch) != cudaSuccess) return OPW_ERR_CUDA;
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-        return OPW_ERR_CUDA;
-    const int grid = (o.num_ctas > 0 && o.num_ctas < sms) ? o.num_ctas : sms;
-    const int max_pairs = ag_max_pairs();
-    if (max_pairs <= 0) return OPW_ERR_CUDA;
-    int pairs = grid / 2 > 0 ? grid / 2 : 1;
-    if (pairs > max_pairs) pairs = max_pairs;
+    const int pairs = ag_pairs_for(o, dev);
+    if (pairs <= 0) return OPW_ERR_CUDA;
 
     int64_t* flags = static_cast<int64_t*>(scratch);
     unsigned long long* counters = static_cast<unsigned long long*>(scratch) + kMaxFlags;
-
     AgParams p;
-    std::memset(&p, 0, sizeof p);
-    char* heap = static_cast<char*>(symm->heap_dev);
-    for (int r = 0; r < R; ++r)
-        if (!make_map(&p.shard[r], heap + symm->rank_off[r] + a_off, K, M_r, static_cast<uint32_t>(ft),
-                      GATHER_SUB_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return OPW_ERR_CUDA;
-    if (!make_map(&p.g_store, G_dev, K, M, static_cast<uint32_t>(ft), GATHER_SUB_ROWS,
-                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&p.g_load, G_dev, K, M, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&p.b_load, B_dev, N, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&p.c_store, C_dev, N, M, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
-        return OPW_ERR_CUDA;
+    const opw_status st_params = ag_fill_params(symm, a_off, M_r, N, K, ft, B_dev, G_dev, C_dev, o, &p);
+    if (st_params != OPW_OK) return st_params;
     p.flags = flags;
     p.status = status_dev;
     p.counters = counters;
-    p.trace = o.trace_dev;
     p.epoch = 1;  // flags were just cleared to 0
-    p.timeout_ns = o.timeout_ns != 0 ? o.timeout_ns : 2000000000ull;
     p.claim_base = 0;
-    p.R = R;
-    p.M_r = static_cast<int32_t>(M_r);
-    p.M = static_cast<int32_t>(M);
-    p.N = static_cast<int32_t>(N);
-    p.K = static_cast<int32_t>(K);
-    p.ft = static_cast<int32_t>(ft);
-    p.T_mr = static_cast<int32_t>(M_r / ft);
-    p.T_k = static_cast<int32_t>(K / ft);
-    p.T_M = static_cast<int32_t>((M + PAIR_M - 1) / PAIR_M);
-    p.T_N = static_cast<int32_t>((N + BN - 1) / BN);
-    p.role = OPW_ROLE_FUSED;
-    p.sync_mode = o.sync_mode;
-    p.schedule = o.schedule;
-    // Row groups only pay when B (K x N bf16) is too big to stay in L2.
-    p.group_rows = (K * N * 2 > (int64_t(64) << 20)) ? 8 : 1;
-    p.signal_mode = o.signal_mode;
-    p.has_perm = o.publish_perm != nullptr;
-    p.has_delay = o.delay_ns != nullptr;
-    p.fault_kind = o.fault_kind;
-    p.fault_arg = o.fault_arg;
-    for (int i = 0; i < R; ++i) {
-        p.perm[i] = o.publish_perm != nullptr ? o.publish_perm[i] : i;
-        p.delay_ns[i] = o.delay_ns != nullptr ? o.delay_ns[i] : 0u;
-        p.rank_target[i] = static_cast<uint64_t>(p.T_mr) * p.T_k;
-    }
+    for (int i = 0; i < R; ++i) p.rank_target[i] = static_cast<uint64_t>(p.T_mr) * p.T_k;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int blocks = static_cast<int>((F + 255) / 256);

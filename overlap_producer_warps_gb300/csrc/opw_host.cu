@@ -124,6 +124,113 @@ int grid_for(const opw_opts& o, int dev)
 
 }  // namespace
 
+// ---------------------------------------------------------------- AG-GEMM set-up
+// Shared by opw_ag_gemm and opw_ag_gemm_noalloc.
+
+namespace opw {
+
+opw_status ag_check_args(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t N, int64_t K,
+                         const void* B_dev, const void* G_dev, const void* C_dev,
+                         const opw_opts& o, int64_t* ft_out)
+{
+    opw_status st = check_symm(symm);
+    if (st != OPW_OK) return st;
+    if (B_dev == nullptr || G_dev == nullptr || C_dev == nullptr) return OPW_ERR_INVALID_ARG;
+    if (o.sync_mode != OPW_SYNC_OVERLAP && o.sync_mode != OPW_SYNC_SERIAL &&
+        o.sync_mode != OPW_SYNC_CHECKED)
+        return OPW_ERR_INVALID_ARG;
+    if (o.schedule != OPW_SCHED_SWIZZLE && o.schedule != OPW_SCHED_READY) return OPW_ERR_INVALID_ARG;
+    if (o.role < OPW_ROLE_FUSED || o.role > OPW_ROLE_CONSUMER) return OPW_ERR_INVALID_ARG;
+    if (o.fault_kind < OPW_FAULT_NONE || o.fault_kind > OPW_FAULT_STALE_EPOCH) return OPW_ERR_INVALID_ARG;
+    if (o.num_ctas < 0) return OPW_ERR_INVALID_ARG;
+    if (o.signal_mode != OPW_SIGNAL_TILE_SET && o.signal_mode != OPW_SIGNAL_ROW_ADD)
+        return OPW_ERR_INVALID_ARG;
+    if (o.reserved != 0) return OPW_ERR_INVALID_ARG;
+    const int R = symm->R;
+    if (o.publish_perm != nullptr) {
+        bool seen[OPW_MAX_RANKS] = {};
+        for (int i = 0; i < R; ++i) {
+            const int r = o.publish_perm[i];
+            if (r < 0 || r >= R || seen[r]) return OPW_ERR_INVALID_ARG;
+            seen[r] = true;
+        }
+    }
+    const int64_t ft = opw_ag_flag_tile(M_r, K);
+    if (ft < 0 || N <= 0 || N % 8 != 0) return OPW_ERR_UNSUPPORTED_SHAPE;
+    const int64_t M = static_cast<int64_t>(R) * M_r;
+    if (M > (int64_t(1) << 31) || N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+        return OPW_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(B_dev) || !aligned16(G_dev) || !aligned16(C_dev) ||
+        !aligned16(static_cast<int64_t>(a_off)) ||
+        (o.trace_dev != nullptr && (reinterpret_cast<uintptr_t>(o.trace_dev) & 7u) != 0))
+        return OPW_ERR_MISALIGNED;
+    *ft_out = ft;
+    return OPW_OK;
+}
+
+int ag_pairs_for(const opw_opts& o, int dev)
+{
+    // CTAs work in pairs: num_ctas (or the SM count) is rounded down to an
+    // even number, at least 2, and capped at what can be resident.
+    const int grid = grid_for(o, dev);
+    if (grid <= 0) return 0;
+    const int max_pairs = ag_max_pairs();
+    if (max_pairs <= 0) return 0;
+    const int pairs = grid / 2 > 0 ? grid / 2 : 1;
+    return pairs < max_pairs ? pairs : max_pairs;
+}
+
+opw_status ag_fill_params(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t N, int64_t K,
+                          int64_t ft, const void* B_dev, void* G_dev, void* C_dev,
+                          const opw_opts& o, AgParams* pp)
+{
+    AgParams& p = *pp;
+    std::memset(&p, 0, sizeof p);
+    const int R = symm->R;
+    const int64_t M = static_cast<int64_t>(R) * M_r;
+    char* heap = static_cast<char*>(symm->heap_dev);
+    for (int r = 0; r < R; ++r) {
+        if (!make_map(&p.shard[r], heap + symm->rank_off[r] + a_off, K, M_r, static_cast<uint32_t>(ft),
+                      GATHER_SUB_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return OPW_ERR_CUDA;
+    }
+    if (!make_map(&p.g_store, G_dev, K, M, static_cast<uint32_t>(ft), GATHER_SUB_ROWS,
+                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&p.g_load, G_dev, K, M, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&p.b_load, B_dev, N, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&p.c_store, C_dev, N, M, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+        return OPW_ERR_CUDA;
+    p.trace = o.trace_dev;
+    p.timeout_ns = o.timeout_ns != 0 ? o.timeout_ns : kDefaultTimeoutNs;
+    p.R = R;
+    p.M_r = static_cast<int32_t>(M_r);
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.ft = static_cast<int32_t>(ft);
+    p.T_mr = static_cast<int32_t>(M_r / ft);
+    p.T_k = static_cast<int32_t>(K / ft);
+    p.T_M = static_cast<int32_t>((M + PAIR_M - 1) / PAIR_M);
+    p.T_N = static_cast<int32_t>((N + BN - 1) / BN);
+    p.role = o.role;
+    p.sync_mode = o.sync_mode;
+    p.schedule = o.schedule;
+    // Row groups only pay when B (K x N bf16) is too big to stay in L2.
+    p.group_rows = (K * N * 2 > (int64_t(64) << 20)) ? 8 : 1;
+    p.signal_mode = o.signal_mode;
+    p.has_perm = o.publish_perm != nullptr;
+    p.has_delay = o.delay_ns != nullptr;
+    p.fault_kind = o.fault_kind;
+    p.fault_arg = o.fault_arg;
+    for (int i = 0; i < R; ++i) {
+        p.perm[i] = o.publish_perm != nullptr ? o.publish_perm[i] : i;
+        p.delay_ns[i] = o.delay_ns != nullptr ? o.delay_ns[i] : 0u;
+    }
+    return OPW_OK;
+}
+
+}  // namespace opw
+
 // ---------------------------------------------------------------- C ABI
 
 extern "C" {
@@ -264,40 +371,13 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
                        uint64_t epoch, const opw_opts* opts_in, void* stream)
 {
     // ---- arguments (no CUDA call before every check has passed)
-    opw_status st = check_symm(symm);
-    if (st != OPW_OK) return st;
-    if (B_dev == nullptr || G_dev == nullptr || C_dev == nullptr || sig == nullptr)
-        return OPW_ERR_INVALID_ARG;
+    if (sig == nullptr) return OPW_ERR_INVALID_ARG;
     opw_opts tmp;
     const opw_opts& o = opts_or_default(opts_in, tmp);
-    if (o.sync_mode != OPW_SYNC_OVERLAP && o.sync_mode != OPW_SYNC_SERIAL &&
-        o.sync_mode != OPW_SYNC_CHECKED)
-        return OPW_ERR_INVALID_ARG;
-    if (o.schedule != OPW_SCHED_SWIZZLE && o.schedule != OPW_SCHED_READY) return OPW_ERR_INVALID_ARG;
-    if (o.role < OPW_ROLE_FUSED || o.role > OPW_ROLE_CONSUMER) return OPW_ERR_INVALID_ARG;
-    if (o.fault_kind < OPW_FAULT_NONE || o.fault_kind > OPW_FAULT_STALE_EPOCH) return OPW_ERR_INVALID_ARG;
-    if (o.num_ctas < 0) return OPW_ERR_INVALID_ARG;
-    if (o.signal_mode != OPW_SIGNAL_TILE_SET && o.signal_mode != OPW_SIGNAL_ROW_ADD)
-        return OPW_ERR_INVALID_ARG;
-    if (o.reserved != 0) return OPW_ERR_INVALID_ARG;
+    int64_t ft = 0;
+    opw_status st = opw::ag_check_args(symm, a_off, M_r, N, K, B_dev, G_dev, C_dev, o, &ft);
+    if (st != OPW_OK) return st;
     const int R = symm->R;
-    if (o.publish_perm != nullptr) {
-        bool seen[OPW_MAX_RANKS] = {};
-        for (int i = 0; i < R; ++i) {
-            const int r = o.publish_perm[i];
-            if (r < 0 || r >= R || seen[r]) return OPW_ERR_INVALID_ARG;
-            seen[r] = true;
-        }
-    }
-    const int64_t ft = opw_ag_flag_tile(M_r, K);
-    if (ft < 0 || N <= 0 || N % 8 != 0) return OPW_ERR_UNSUPPORTED_SHAPE;
-    const int64_t M = static_cast<int64_t>(R) * M_r;
-    if (M > (int64_t(1) << 31) || N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
-        return OPW_ERR_UNSUPPORTED_SHAPE;
-    if (!aligned16(B_dev) || !aligned16(G_dev) || !aligned16(C_dev) ||
-        !aligned16(static_cast<int64_t>(a_off)) ||
-        (o.trace_dev != nullptr && (reinterpret_cast<uintptr_t>(o.trace_dev) & 7u) != 0))
-        return OPW_ERR_MISALIGNED;
     const bool row_add = o.signal_mode == OPW_SIGNAL_ROW_ADD;
     const int64_t F = static_cast<int64_t>(R) * (M_r / ft) * (row_add ? 1 : K / ft);
     if (sig->num_slots < F) return OPW_ERR_INVALID_ARG;
@@ -312,60 +392,16 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
     // ---- launch
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != sig->device) return OPW_ERR_CUDA;
-    // CTAs work in pairs: num_ctas (or the SM count) is rounded down to an
-    // even number, at least 2, and capped at what can be resident.
-    const int grid = grid_for(o, dev);
-    if (grid <= 0) return OPW_ERR_CUDA;
-    const int max_pairs = ag_max_pairs();
-    if (max_pairs <= 0) return OPW_ERR_CUDA;
-    int pairs = grid / 2 > 0 ? grid / 2 : 1;
-    if (pairs > max_pairs) pairs = max_pairs;
-
+    const int pairs = opw::ag_pairs_for(o, dev);
+    if (pairs <= 0) return OPW_ERR_CUDA;
     AgParams p;
-    std::memset(&p, 0, sizeof p);
-    char* heap = static_cast<char*>(symm->heap_dev);
-    for (int r = 0; r < R; ++r) {
-        if (!make_map(&p.shard[r], heap + symm->rank_off[r] + a_off, K, M_r, static_cast<uint32_t>(ft),
-                      GATHER_SUB_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return OPW_ERR_CUDA;
-    }
-    if (!make_map(&p.g_store, G_dev, K, M, static_cast<uint32_t>(ft), GATHER_SUB_ROWS,
-                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&p.g_load, G_dev, K, M, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&p.b_load, B_dev, N, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&p.c_store, C_dev, N, M, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
-        return OPW_ERR_CUDA;
+    st = opw::ag_fill_params(symm, a_off, M_r, N, K, ft, B_dev, G_dev, C_dev, o, &p);
+    if (st != OPW_OK) return st;
     p.flags = sig->flags;
     p.status = sig->status;
     p.counters = sig->counters;
-    p.trace = o.trace_dev;
     p.epoch = epoch;
-    p.timeout_ns = o.timeout_ns != 0 ? o.timeout_ns : kDefaultTimeoutNs;
     p.claim_base = sig->claim_next;
-    p.R = R;
-    p.M_r = static_cast<int32_t>(M_r);
-    p.M = static_cast<int32_t>(M);
-    p.N = static_cast<int32_t>(N);
-    p.K = static_cast<int32_t>(K);
-    p.ft = static_cast<int32_t>(ft);
-    p.T_mr = static_cast<int32_t>(M_r / ft);
-    p.T_k = static_cast<int32_t>(K / ft);
-    p.T_M = static_cast<int32_t>((M + PAIR_M - 1) / PAIR_M);
-    p.T_N = static_cast<int32_t>((N + BN - 1) / BN);
-    p.role = o.role;
-    p.sync_mode = o.sync_mode;
-    p.schedule = o.schedule;
-    // Row groups only pay when B (K x N bf16) is too big to stay in L2.
-    p.group_rows = (K * N * 2 > (int64_t(64) << 20)) ? 8 : 1;
-    p.signal_mode = o.signal_mode;
-    p.has_perm = o.publish_perm != nullptr;
-    p.has_delay = o.delay_ns != nullptr;
-    p.fault_kind = o.fault_kind;
-    p.fault_arg = o.fault_arg;
-    for (int i = 0; i < R; ++i) {
-        p.perm[i] = o.publish_perm != nullptr ? o.publish_perm[i] : i;
-        p.delay_ns[i] = o.delay_ns != nullptr ? o.delay_ns[i] : 0u;
-    }
     const uint64_t per_rank = static_cast<uint64_t>(p.T_mr) * p.T_k;
     for (int r = 0; r < R; ++r)
         p.rank_target[r] = produces ? sig->rank_done[r] + per_rank : sig->rank_target_last[r];

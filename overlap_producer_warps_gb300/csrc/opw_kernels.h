@@ -108,6 +108,19 @@ size_t rs_smem_bytes();
 
 // Launch helpers (cooperative launch so every CTA is co-resident).
 int ag_max_pairs();  // clusters of 2 AG-GEMM CTAs that fit at once (0 on error)
+
+// AG-GEMM host set-up shared by the two entry points (opw_host.cu).
+// ag_check_args: every argument check that needs no CUDA call; *ft = flag tile.
+opw_status ag_check_args(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t N, int64_t K,
+                         const void* B_dev, const void* G_dev, const void* C_dev,
+                         const opw_opts& o, int64_t* ft);
+// CTA pairs to launch for these options on device `dev` (0 on error).
+int ag_pairs_for(const opw_opts& o, int dev);
+// Tensor maps, shapes and options of the launch; the caller sets flags,
+// status, counters, epoch, claim_base and rank_target.
+opw_status ag_fill_params(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t N, int64_t K,
+                          int64_t ft, const void* B_dev, void* G_dev, void* C_dev,
+                          const opw_opts& o, AgParams* p);
 cudaError_t launch_ag_gemm(const AgParams& p, int pairs, cudaStream_t s);
 int rs_max_pairs();  // clusters of 2 GEMM-RS CTAs that fit at once (0 on error)
 cudaError_t launch_gemm_rs(const RsParams& p, int pairs, cudaStream_t s);
