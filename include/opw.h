@@ -380,9 +380,9 @@ opw_status opw_ring_allreduce(const opw_symm* symm, size_t data_off, size_t recv
  * README, Tier-2 all-to-all): rank r's send buffer holds R slices of
  * bytes_per_peer bytes at heap_dev + rank_off[r] + send_off; afterwards
  * rank j's receive buffer (recv_off, R slices) holds at slot r the slice j of
- * rank r's send buffer.  Slices move in 8 KiB pieces; each piece sent to a
+ * rank r's send buffer.  Slices move in 32 KiB pieces; each piece sent to a
  * peer is announced by flag slot (j*R + r)*P + piece = epoch (.gpu release),
- * P = ceil(bytes_per_peer / 8192), and every receiver acquires all of its
+ * P = ceil(bytes_per_peer / 32768), and every receiver acquires all of its
  * incoming flags (>= epoch) before the call completes.  The rank's own slice
  * is copied without a flag.
  *

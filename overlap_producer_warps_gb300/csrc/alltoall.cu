@@ -4,8 +4,8 @@
 // and waits until each peer's slice has arrived in its own buffer).
 //
 // On one GPU every rank's send and receive buffers are slices of the heap.
-// A slice of B bytes is cut into 8 KiB pieces; a warp copies one piece
-// (16-byte loads and stores that bypass L1) and, for a peer, releases the
+// A slice of B bytes is cut into 32 KiB pieces; a warp copies one piece, 8 KiB
+// at a time (16-byte loads and stores that bypass L1), and, for a peer, releases the
 // flag of (receiver j, sender r, piece) with the epoch.  The receiving side
 // then acquires every incoming flag (>= epoch, bounded wait): the
 // "wait_signal" of the page.  All warps are co-resident (cooperative launch)
@@ -19,8 +19,9 @@ namespace opw {
 namespace {
 
 constexpr int A2A_THREADS = 256;
-constexpr int A2A_PIECE = 8192;                 // bytes per warp action
-constexpr int A2A_VEC = A2A_PIECE / 16 / 32;    // uint4 per lane (16)
+constexpr int A2A_PIECE = 32768;               // bytes per warp action (one flag)
+constexpr int A2A_CHUNK = 8192;                // bytes one warp holds in registers at once
+constexpr int A2A_VEC = A2A_CHUNK / 16 / 32;   // uint4 per lane (16)
 
 struct A2aParams {
     char* heap;
@@ -34,7 +35,7 @@ struct A2aParams {
     uint64_t timeout_ns;
 };
 
-__device__ __forceinline__ void copy_piece(const char* src, char* dst, int len)
+__device__ __forceinline__ void copy_chunk(const char* src, char* dst, int len)
 {
     const uint32_t lane = lane_id();
     uint4 v[A2A_VEC];
@@ -48,6 +49,14 @@ __device__ __forceinline__ void copy_piece(const char* src, char* dst, int len)
         const int idx = static_cast<int>(lane) + 32 * k;
         if (16 * idx < len) __stcg(reinterpret_cast<uint4*>(dst) + idx, v[k]);
     }
+}
+
+// One release per 32 KiB rather than per 8 KiB: each release waits for the
+// warp's stores to be performed, so fewer of them keep more bytes in flight.
+__device__ __forceinline__ void copy_piece(const char* src, char* dst, int len)
+{
+    for (int o = 0; o < len; o += A2A_CHUNK)
+        copy_chunk(src + o, dst + o, len - o < A2A_CHUNK ? len - o : A2A_CHUNK);
 }
 
 __global__ void __launch_bounds__(A2A_THREADS) alltoall_kernel(const __grid_constant__ A2aParams p)

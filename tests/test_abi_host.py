@@ -110,7 +110,7 @@ def test_flag_geometry(api):
     assert api.ring_num_flags(3, 3 * 400) == 3 * 4 * 1
     assert api.ring_num_flags(3, 1001) == -1
     assert api.ring_recv_bytes(8, 8 * 4096) == 14 * 4096 * 4
-    assert api.alltoall_num_flags(8, 65536) == 8 * 8 * 8       # 8 KiB pieces
+    assert api.alltoall_num_flags(8, 65536) == 8 * 8 * 2       # 32 KiB pieces
     assert api.alltoall_num_flags(3, 48) == 9
     assert api.alltoall_num_flags(3, 40) == -1
     F, T = 2048, 32 * 16  # 256x256 pair tiles

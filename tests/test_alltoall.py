@@ -24,7 +24,7 @@ def api():
 @pytest.mark.parametrize("R,B,order", [
     (2, 4096, None),
     (3, 48, (1, 2, 0)),               # less than one piece per slice
-    (4, 3 * 8192 + 1040, (3, 0, 2, 1)),  # several pieces and a ragged tail
+    (4, 3 * 32768 + 1040, (3, 0, 2, 1)),  # several pieces and a ragged tail
     (8, 65536, None),
     (1, 1024, None),
 ])
