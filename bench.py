@@ -376,8 +376,6 @@ def per_config_results(api, torch, peak_tflops, reps=5):
             api.ag_gemm(heap, d["rank_off"], d["a_off"], M_r, N, K, B, G, C, sig,
                         sig.next_epoch(), api.make_opts(role=api.ROLE_PRODUCER, **skew))
 
-        state = {}
-
         def consumer_only():
             api.ag_gemm(heap, d["rank_off"], d["a_off"], M_r, N, K, B, G, C, sig,
                         sig.next_epoch() - 1, api.make_opts(role=api.ROLE_CONSUMER, **skew))
@@ -391,6 +389,10 @@ def per_config_results(api, torch, peak_tflops, reps=5):
                         sig_add.next_epoch(), api.make_opts(signal_mode=api.SIGNAL_ROW_ADD, **skew))
 
         t_add = time_launches(torch, fused_row_add, reps)
+        # the skew layer with its publish order but without the per-rank delays
+        t_nodelay = (time_launches(torch, lambda: api.ag_gemm(
+            heap, d["rank_off"], d["a_off"], M_r, N, K, B, G, C, sig, sig.next_epoch(),
+            api.make_opts(publish_perm=skew["publish_perm"])), reps) if skew else None)
         if sig_add.status()[0] != api.OK:
             raise RuntimeError(f"{name}: device error with row-ADD signals")
         sig_add.close()
@@ -422,6 +424,9 @@ def per_config_results(api, torch, peak_tflops, reps=5):
             "overlap_efficiency": max(0.0, min(1.0, e)),
             "gather_hbm_gbs_producer_only": 2.0 * M * K * 2 / (t_prod * 1e-3) / 1e9,
         }
+        if t_nodelay is not None:
+            out[name]["no_delay_fused_tflops"] = fl / t_nodelay / 1e9
+            out[name]["ms"]["no_delay"] = t_nodelay
         sig.close()
         del heap, B, G, C, shards
         torch.cuda.empty_cache()
@@ -608,8 +613,9 @@ def run_ours(args, rank, world, dist):
     clocks = sampler.stop()
     w.check()
     ms_total = start.elapsed_time(end)
-    ag_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    rs_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    ag_all = [e[0].elapsed_time(e[1]) for e in evs]
+    rs_all = [e[1].elapsed_time(e[2]) for e in evs]
+    ag_ms, rs_ms = statistics.mean(ag_all), statistics.mean(rs_all)
     t_step = reduce_max(ms_total / args.steps, dist, "cuda")
     flops_step = w.flops_ag + w.flops_rs
     value = whole_job_tflops(world, flops_step, t_step)
@@ -626,7 +632,10 @@ def run_ours(args, rank, world, dist):
                 "unit": "TFLOP/s", "frac": achieved / step_peak,
                 "peak_source": f"{peak_src} {step_peak_name}",
                 "traffic": kernel_traffic(dom),
-                "ms_per_launch": {"ag_gemm": ag_ms, "gemm_rs": rs_ms}}
+                "ms_per_launch": {"ag_gemm": ag_ms, "gemm_rs": rs_ms},
+                "ms_per_launch_median": {"ag_gemm": statistics.median(ag_all),
+                                         "gemm_rs": statistics.median(rs_all)},
+                "ms_per_launch_min": {"ag_gemm": min(ag_all), "gemm_rs": min(rs_all)}}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True,
