@@ -160,6 +160,31 @@ def test_fewer_ctas_than_sms(api):
     _run_and_check(api, d, opts_fn=lambda i: api.make_opts(num_ctas=5))
 
 
+def test_one_pair_claims_every_tile(api):
+    """num_ctas=2: a single CTA pair claims all 32 pair tiles from the ready
+    counter while every CTA's producer warp (two of them) gathers."""
+    d = inputs.ag_inputs(_cfg(4, 512, 256, 1024), seed=16)
+    _run_and_check(api, d, epoch_runs=2, opts_fn=lambda i: api.make_opts(num_ctas=2))
+
+
+def test_grouped_ready_order_with_ragged_group(api):
+    """K*N*2 > 64 MiB switches the ready order to groups of 8 pair rows with
+    the column index outermost; 9 pair rows leave a ragged last group of 1."""
+    R, M_r, K, N = 3, 768, 8192, 4224            # M = 2304 rows = 9 pair rows
+    assert K * N * 2 > 64 << 20
+    d = inputs.ag_inputs(_cfg(R, M_r, K, N), seed=17)
+    prob = AgProblem(d)
+    sig = api.Signal(api.ag_num_flags(R, M_r, K))
+    for _ in range(2):
+        prob.run(api, sig, sig.next_epoch())
+        assert sig.status()[0] == api.OK
+    G = host_bits(prob.G)
+    assert np.array_equal(G, oracle.allgather(d["heap"], d["rank_off"], R, d["a_off"], M_r, K))
+    rows = sample_rows(prob.M, 128, 1, seed=5)
+    C = host_bits(prob.C)
+    assert_gemm_close(C[rows], prob.oracle_rows(rows), what="grouped order C")
+
+
 def _trace_views(api, prob, trace, grid):
     F = api.ag_num_flags(prob.R, prob.M_r, prob.K)
     T = ((prob.M + 255) // 256) * ((prob.N + 255) // 256)  # 256x256 pair tiles
