@@ -669,6 +669,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--prewarm-s", type=float, default=2.0,
                     help="seconds of untimed steps before the warm-up steps (clock ramp)")
+    ap.add_argument("--only", choices=["ring_allreduce", "alltoall"], default=None,
+                    help="run only this per-configuration measurement (for profiling) and "
+                         "print its result as one JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -678,6 +681,12 @@ def main():
     dist = None
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.only is not None:
+        import torch
+        from overlap_producer_warps_gb300 import api
+        fn = ring_results if args.only == "ring_allreduce" else alltoall_results
+        print(json.dumps({args.only: fn(api, torch, args.steps)}), flush=True)
+        return 0
     if world > 1:
         import torch
         import torch.distributed as _dist
