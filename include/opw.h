@@ -192,7 +192,9 @@ typedef struct {
     int32_t fault_kind;           /* OPW_FAULT_* (fault injection on the host-chosen slot) */
     int32_t fault_arg;
     int32_t signal_mode;          /* OPW_SIGNAL_* (AG-GEMM only) */
-    int32_t reserved;             /* must be 0 */
+    int32_t local_rank;           /* AG-GEMM: the logical rank the consumer plays, whose own
+                                     shard is local (default 0); -1: none.  Other calls
+                                     accept 0 or -1 and ignore it.  See opw_ag_gemm. */
 } opw_opts;
 
 /* Fill *o with the defaults (all fields 0 / NULL). */
@@ -248,6 +250,11 @@ int64_t opw_ag_trace_words(int32_t R, int64_t M_r, int64_t N, int64_t K);
  *
  * Producer warps copy each flag tile of each A_r into G with TMA, wait for the
  * copy to complete, then publish flags[slot] = epoch with a .gpu release.
+ * The GPU plays the consumer of rank opts.local_rank (default 0): that rank's
+ * own shard is local, so consumers read its rows in place from A_local and
+ * never wait on its flags, and they take its tiles first.  Its tiles are still
+ * copied into G (after every other rank's) and published.  With local_rank =
+ * -1 every tile is read from G after its flag.
  * Consumers, in CTA pairs working on 256x256 output tiles, acquire each flag
  * (>= epoch) before their TMA loads read that tile of G, then run tcgen05
  * cta_group::2 MMAs with TMEM accumulators.  After the launch every flag slot

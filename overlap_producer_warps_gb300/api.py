@@ -51,7 +51,7 @@ class Opts(ctypes.Structure):
                 ("delay_ns", ctypes.POINTER(ctypes.c_uint32)),
                 ("trace_dev", ctypes.c_void_p), ("fault_kind", ctypes.c_int32),
                 ("fault_arg", ctypes.c_int32), ("signal_mode", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("local_rank", ctypes.c_int32)]
 
 
 _vp = ctypes.c_void_p
@@ -195,7 +195,7 @@ class Signal:
 
 def make_opts(timeout_ns=0, sync_mode=SYNC_OVERLAP, schedule=SCHED_READY, role=ROLE_FUSED,
               num_ctas=0, publish_perm=None, delay_ns=None, trace=None, fault_kind=FAULT_NONE,
-              fault_arg=0, signal_mode=SIGNAL_TILE_SET):
+              fault_arg=0, signal_mode=SIGNAL_TILE_SET, local_rank=0):
     """Build an Opts struct; array arguments are kept alive on the struct."""
     o = Opts()
     lib().opw_opts_default(ctypes.byref(o))
@@ -218,6 +218,7 @@ def make_opts(timeout_ns=0, sync_mode=SYNC_OVERLAP, schedule=SCHED_READY, role=R
     o.fault_kind = int(fault_kind)
     o.fault_arg = int(fault_arg)
     o.signal_mode = int(signal_mode)
+    o.local_rank = int(local_rank)
     o._keep = keep
     return o
 

@@ -13,8 +13,9 @@
 // receives its 128 accumulator rows in its own TMEM.  8 warps per CTA:
 //   warp 0     loader (both CTAs): takes tiles from the on-chip tile queue and
 //              TMA-loads this CTA's half of their A k-blocks (from the gathered
-//              buffer G) and B k-blocks into a 5-stage ring; the bytes of both
-//              halves complete on the even CTA's `full` barrier.
+//              buffer G, or in place from the local rank's own shard) and B
+//              k-blocks into a 5-stage ring; the bytes of both halves complete
+//              on the even CTA's `full` barrier.
 //   warp 1     MMA (even CTA only): one thread issues the pair's tcgen05.mma
 //              (bf16 x bf16 -> fp32) into a double-buffered TMEM accumulator
 //              (2 x 128 lanes x 256 columns in each CTA).
@@ -23,10 +24,14 @@
 //              publishes the tile's flag with st.release.gpu.
 //   warp 3     allocates / frees the pair's TMEM; in the even CTA it is also
 //              the scheduler: it picks the next output tile, acquires
-//              (ld.acquire.gpu) the flags of all the A rows that tile needs,
-//              and only then puts it on both CTAs' tile queues.  Acquiring
-//              ahead of the loaders keeps every global-memory round trip off
-//              the k-block loop.
+//              (ld.acquire.gpu) the flags of all the A rows that tile needs
+//              (none for the local rank's rows, which are read in place), and
+//              only then puts it on both CTAs' tile queues.  Acquiring ahead
+//              of the loaders keeps every global-memory round trip off the
+//              k-block loop.
+// The GPU plays the consumer of rank p.local_rank (or none, -1): that rank's
+// shard is local, so its tiles are taken first and its own flags are never
+// waited for; its producer copies still fill G, after every other rank's.
 //   warps 4-7  epilogue (both CTAs): tcgen05.ld -> bf16 (round to nearest
 //              even) -> swizzled shared memory -> TMA store of C.
 // Every wait is bounded: on timeout the kernel latches an error in the
@@ -123,7 +128,27 @@ __device__ __forceinline__ int ready_tile(const AgParams& p, int idx)
     int m = mp;
     if (p.ft == BM && p.M_r % PAIR_M == 0) {
         const int tpr = p.M_r / PAIR_M;
-        if (p.has_perm) {
+        if (p.local_rank >= 0 && p.R > 1) {
+            // the local rank's rows first (no wait), then the others in publish order
+            if (mp < tpr) {
+                m = p.local_rank * tpr + mp;
+            } else {
+                const int j = mp - tpr;
+                if (p.has_perm) {
+                    int ip = j / tpr;  // position among the other ranks in publish order
+                    int r = -1;
+                    for (int i = 0, seen = 0; i < p.R; ++i)
+                        if (p.perm[i] != p.local_rank) {
+                            if (seen == ip) { r = p.perm[i]; break; }
+                            ++seen;
+                        }
+                    m = r * tpr + j % tpr;
+                } else {
+                    const int k = j / (p.R - 1), ri = j % (p.R - 1);
+                    m = (ri < p.local_rank ? ri : ri + 1) * tpr + k;
+                }
+            }
+        } else if (p.has_perm) {
             m = p.perm[mp / tpr] * tpr + mp % tpr;
         } else {
             m = (mp % p.R) * tpr + mp / p.R;
@@ -259,6 +284,15 @@ __device__ __forceinline__ void flag_rows(const AgParams& p, int m0, int& base0,
     }
 }
 
+// Rows [m0, m0 + 128) all belong to the consumer's own rank: read them from
+// its shard in place, without any flag.
+__device__ __forceinline__ bool local_half(const AgParams& p, int m0)
+{
+    if (p.local_rank < 0) return false;
+    const int last = (m0 + BM <= p.M ? m0 + BM : p.M) - 1;
+    return m0 / p.M_r == p.local_rank && last / p.M_r == p.local_rank;
+}
+
 struct LoaderRing {
     uint32_t stage = 0, sphase = 0, filled = 0, last_par = 0;
 };
@@ -267,7 +301,8 @@ struct LoaderRing {
 // tile (A rows from m0, B columns from n0): the plain GEMM pipeline, with
 // nothing else in the loop.
 __device__ __forceinline__ bool issue_kblocks(const AgParams& p, uint8_t* smem, AgCtrl* ctrl,
-                                              const ErrCtx& ec, LoaderRing& rg, int m0, int n0,
+                                              const ErrCtx& ec, LoaderRing& rg,
+                                              const CUtensorMap* amap, int m0, int n0,
                                               int kb0, int kb1, uint32_t crank)
 {
     const uint32_t lane = lane_id();
@@ -276,7 +311,7 @@ __device__ __forceinline__ bool issue_kblocks(const AgParams& p, uint8_t* smem, 
         if (lane == 0) {
             const uint32_t fb = mapa_shared(smem_u32(&ctrl->full[rg.stage]), 0);
             if (crank == 0) mbar_arrive_expect_tx(&ctrl->full[rg.stage], PAIR_TX_BYTES);
-            tma_load_2d_pair(smem + OFF_A + rg.stage * A_STAGE_BYTES, &p.g_load, fb, kb * BK, m0);
+            tma_load_2d_pair(smem + OFF_A + rg.stage * A_STAGE_BYTES, amap, fb, kb * BK, m0);
             uint8_t* bs = smem + OFF_B + rg.stage * B_HALF_BYTES;
 #pragma unroll
             for (int j = 0; j < HALF_N / 64; ++j)
@@ -356,6 +391,7 @@ __device__ void run_scheduler(const AgParams& p, AgCtrl* ctrl, const ErrCtx& ec)
             for (int half = 0; half < 2; ++half) {
                 const int m0 = (q / p.T_N) * PAIR_M + half * BM;
                 if (m0 >= p.M) break;
+                if (local_half(p, m0)) continue;  // read in place: nothing to wait for
                 int base0, base1;
                 flag_rows(p, m0, base0, base1);
                 int ready_kt = 0;
@@ -401,10 +437,13 @@ __device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
         __syncwarp();
         const int m0 = (q / p.T_N) * PAIR_M + static_cast<int>(crank) * BM;
         const int n0 = (q % p.T_N) * BN + static_cast<int>(crank) * HALF_N;
+        const bool loc = local_half(p, m0);
+        const CUtensorMap* amap = loc ? &p.a_local_load : &p.g_load;
+        const int ay = loc ? m0 - p.local_rank * p.M_r : m0;
         const int kb_ask = KB > CLAIM_LEAD_KB ? KB - CLAIM_LEAD_KB : 0;
-        if (!issue_kblocks(p, smem, ctrl, ec, rg, m0, n0, 0, kb_ask, crank)) break;
+        if (!issue_kblocks(p, smem, ctrl, ec, rg, amap, ay, n0, 0, kb_ask, crank)) break;
         if (crank == 0 && lane == 0) mbar_arrive(&ctrl->need_next);
-        if (!issue_kblocks(p, smem, ctrl, ec, rg, m0, n0, kb_ask, KB, crank)) break;
+        if (!issue_kblocks(p, smem, ctrl, ec, rg, amap, ay, n0, kb_ask, KB, crank)) break;
     }
     // The even CTA's `full` phases cover both CTAs' loads: every armed one
     // must complete before the pair may exit.
@@ -559,11 +598,22 @@ __device__ void run_gather(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
             mt = rem / p.T_k;
             kt = rem - mt * p.T_k;
         } else {
-            // row block by row block, ranks interleaved, k fastest
-            mt = pidx / (p.R * p.T_k);
-            const int rem = pidx - mt * p.R * p.T_k;
-            r = rem / p.T_k;
-            kt = rem - r * p.T_k;
+            // row block by row block, ranks interleaved, k fastest; the
+            // consumer's own rank (read in place) last
+            const int others = p.local_rank >= 0 ? (p.R - 1) * per_rank : n_items;
+            if (pidx < others) {
+                const int Ro = p.local_rank >= 0 ? p.R - 1 : p.R;
+                mt = pidx / (Ro * p.T_k);
+                const int rem = pidx - mt * Ro * p.T_k;
+                const int ri = rem / p.T_k;
+                r = (p.local_rank >= 0 && ri >= p.local_rank) ? ri + 1 : ri;
+                kt = rem - ri * p.T_k;
+            } else {
+                const int j = pidx - others;
+                r = p.local_rank;
+                mt = j / p.T_k;
+                kt = j - mt * p.T_k;
+            }
         }
 
         // Skewed readiness: rank r starts no earlier than delay_ns[r] ...

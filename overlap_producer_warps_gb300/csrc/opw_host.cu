@@ -145,8 +145,8 @@ opw_status ag_check_args(const opw_symm* symm, size_t a_off, int64_t M_r, int64_
     if (o.num_ctas < 0) return OPW_ERR_INVALID_ARG;
     if (o.signal_mode != OPW_SIGNAL_TILE_SET && o.signal_mode != OPW_SIGNAL_ROW_ADD)
         return OPW_ERR_INVALID_ARG;
-    if (o.reserved != 0) return OPW_ERR_INVALID_ARG;
     const int R = symm->R;
+    if (o.local_rank < -1 || o.local_rank >= R) return OPW_ERR_INVALID_ARG;
     if (o.publish_perm != nullptr) {
         bool seen[OPW_MAX_RANKS] = {};
         for (int i = 0; i < R; ++i) {
@@ -199,6 +199,11 @@ opw_status ag_fill_params(const opw_symm* symm, size_t a_off, int64_t M_r, int64
         !make_map(&p.g_load, G_dev, K, M, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&p.b_load, B_dev, N, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&p.c_store, C_dev, N, M, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+        return OPW_ERR_CUDA;
+    p.local_rank = o.local_rank;
+    if (o.local_rank >= 0 &&
+        !make_map(&p.a_local_load, heap + symm->rank_off[o.local_rank] + a_off, K, M_r, 64, BM,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
         return OPW_ERR_CUDA;
     p.trace = o.trace_dev;
     p.timeout_ns = o.timeout_ns != 0 ? o.timeout_ns : kDefaultTimeoutNs;
@@ -441,7 +446,7 @@ opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t 
     const opw_opts& o = opts_or_default(opts_in, tmp);
     if ((o.sync_mode != OPW_SYNC_OVERLAP && o.sync_mode != OPW_SYNC_CHECKED) || o.schedule != 0 ||
         o.role != 0 || o.publish_perm != nullptr || o.delay_ns != nullptr || o.fault_kind != 0 ||
-        o.num_ctas < 0 || o.signal_mode != 0 || o.reserved != 0)
+        o.num_ctas < 0 || o.signal_mode != 0 || o.local_rank < -1 || o.local_rank > 0)
         return OPW_ERR_INVALID_ARG;
     const int R = symm->R;
     if (M <= 0 || N <= 0 || K_r <= 0 || M % (128 * R) != 0 || N % 8 != 0 || K_r % 8 != 0)

@@ -51,6 +51,7 @@ struct AgParams {
     CUtensorMap g_load;                // G [M, K], box {64, 128}, 128B swizzle (consumer A)
     CUtensorMap b_load;                // B [K, N], box {64, 64}, 128B swizzle (consumer B)
     CUtensorMap c_store;               // C [M, N], box {64, 32}, 128B swizzle (epilogue)
+    CUtensorMap a_local_load;          // A_local [M_r, K], box {64, 128}, 128B swizzle (consumer A)
     int64_t* flags;
     int32_t* status;
     unsigned long long* counters;
@@ -65,6 +66,7 @@ struct AgParams {
     int32_t role, sync_mode, schedule;
     int32_t group_rows;       // dynamic schedule: row tiles per rasterisation group
     int32_t signal_mode;      // OPW_SIGNAL_TILE_SET or OPW_SIGNAL_ROW_ADD
+    int32_t local_rank;       // the consumer's own rank (read in place, no flag wait), or -1
     int32_t has_perm, has_delay;
     int32_t fault_kind, fault_arg;
     int32_t perm[OPW_MAX_RANKS];

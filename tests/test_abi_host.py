@@ -55,7 +55,7 @@ int main(void) {
     offsetof(opw_opts, timeout_ns), offsetof(opw_opts, sync_mode), offsetof(opw_opts, schedule),
     offsetof(opw_opts, role), offsetof(opw_opts, num_ctas), offsetof(opw_opts, publish_perm),
     offsetof(opw_opts, delay_ns), offsetof(opw_opts, trace_dev), offsetof(opw_opts, fault_kind),
-    offsetof(opw_opts, fault_arg), offsetof(opw_opts, signal_mode), offsetof(opw_opts, reserved));
+    offsetof(opw_opts, fault_arg), offsetof(opw_opts, signal_mode), offsetof(opw_opts, local_rank));
   printf("%zu %zu %zu %zu %zu\n", sizeof(opw_symm), offsetof(opw_symm, heap_dev),
     offsetof(opw_symm, rank_off), offsetof(opw_symm, R), offsetof(opw_symm, reserved));
   return 0;
@@ -167,6 +167,8 @@ def test_ag_gemm_rejects_bad_arguments_on_the_host(api):
     assert _ag(api, opts=api.make_opts(publish_perm=[0, 0])) == E.ERR_INVALID_ARG
     assert _ag(api, opts=api.make_opts(publish_perm=[0, 2])) == E.ERR_INVALID_ARG
     assert _ag(api, opts=api.make_opts(signal_mode=2)) == E.ERR_INVALID_ARG
+    assert _ag(api, opts=api.make_opts(local_rank=-2)) == E.ERR_INVALID_ARG
+    assert _ag(api, opts=api.make_opts(local_rank=2)) == E.ERR_INVALID_ARG   # R = 2
     # a signal object with too few slots (here: none)
     assert _ag(api) == E.ERR_INVALID_ARG
 

@@ -185,6 +185,20 @@ def test_grouped_ready_order_with_ragged_group(api):
     assert_gemm_close(C[rows], prob.oracle_rows(rows), what="grouped order C")
 
 
+@pytest.mark.parametrize("R,M_r,K,N", [(4, 512, 512, 768), (3, 192, 320, 264)])
+def test_local_rank_choice_does_not_change_results(api, R, M_r, K, N):
+    """Reading the local rank's shard in place (and taking its tiles first) or
+    waiting on every rank's flags computes the same G, C and flags bit for bit."""
+    d = inputs.ag_inputs(_cfg(R, M_r, K, N), seed=18 + R)
+    outs = []
+    for local in (-1, 0, R - 1):
+        prob = _run_and_check(api, d, epoch_runs=2, full=(local == -1),
+                              opts_fn=lambda i, local=local: api.make_opts(local_rank=local))
+        outs.append((host_bits(prob.G), host_bits(prob.C)))
+    for G, C in outs[1:]:
+        assert np.array_equal(G, outs[0][0]) and np.array_equal(C, outs[0][1])
+
+
 def _trace_views(api, prob, trace, grid):
     F = api.ag_num_flags(prob.R, prob.M_r, prob.K)
     T = ((prob.M + 255) // 256) * ((prob.N + 255) // 256)  # 256x256 pair tiles
@@ -206,9 +220,14 @@ def test_trace_publish_before_consume_and_swizzle_order(api):
                                                        schedule=api.SCHED_SWIZZLE))
     assert sig.status()[0] == api.OK
     v = _trace_views(api, prob, trace, grid)
-    # every tile published, and no consumer acquired a tile before its publish
-    assert np.all(v["publish"] > 0) and np.all(v["consume"] != np.uint64(2 ** 64 - 1))
-    assert np.all(v["publish"] <= v["consume"])
+    # every tile published; every tile of another rank acquired no earlier than
+    # its publish; the local rank's own tiles (rank 0 by default) never acquired
+    per_rank = v["F"] // R
+    remote = np.arange(v["F"]) >= per_rank
+    assert np.all(v["publish"] > 0)
+    assert np.all(v["consume"][remote] != np.uint64(2 ** 64 - 1))
+    assert np.all(v["publish"][remote] <= v["consume"][remote])
+    assert np.all(v["consume"][~remote] == np.uint64(2 ** 64 - 1))
     # each consumer (a CTA pair) visited its 256x256 tiles in the oracle's
     # swizzled order
     T_M, T_N, pairs = prob.M // 256, (N + 255) // 256, grid // 2

@@ -149,3 +149,27 @@ def test_gemm_rs_checked_publish_finds_the_previous_epoch(api):
     sig.reset()
     prob.run(api, sig, sig.next_epoch(), opts)
     assert sig.status()[0] == api.OK
+
+
+def test_local_rank_tiles_are_not_waited_for(api):
+    """The consumer reads its own rank's shard in place: a flag of that rank
+    that is never published delays nobody (the launch completes and C is
+    right), while the same drop with local_rank=-1 times out."""
+    prob = _problem(seed=42)
+    F = api.ag_num_flags(4, 128, 256)
+    slot = 1                                  # rank 0's second flag tile
+    sig = api.Signal(F)
+    prob.run(api, sig, sig.next_epoch(), api.make_opts(timeout_ns=TIMEOUT_NS, local_rank=0,
+                                                       fault_kind=api.FAULT_DROP_TILE,
+                                                       fault_arg=slot))
+    assert sig.status()[0] == api.OK
+    flags = sig.flags().cpu().numpy()
+    assert flags[slot] == 0 and np.all(np.delete(flags, slot) == 1)
+    G_ref, C_ref = prob.oracle_full()
+    assert np.array_equal(host_bits(prob.G), G_ref)
+    assert_gemm_close(host_bits(prob.C), C_ref)
+    sig2 = api.Signal(F)
+    prob.run(api, sig2, sig2.next_epoch(), api.make_opts(timeout_ns=TIMEOUT_NS, local_rank=-1,
+                                                         fault_kind=api.FAULT_DROP_TILE,
+                                                         fault_arg=slot))
+    assert sig2.status() == (api.ERR_TIMEOUT, 0, slot)
