@@ -38,6 +38,7 @@
 // signal object's status word, drains its own in-flight copies and MMAs,
 // frees TMEM and returns.  Cluster barriers bracket the kernel, so neither CTA
 // of a pair leaves while the other may still use its shared memory or TMEM.
+#include <atomic>
 #include <cstdlib>
 
 #include "opw_device.cuh"
@@ -842,7 +843,7 @@ cudaLaunchConfig_t pair_config(unsigned pairs, cudaStream_t s, cudaLaunchAttribu
 
 bool set_smem_attr()
 {
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64] = {};  // per device; set once, benign repeats
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     if (!attr_set[dev]) {
@@ -860,10 +861,10 @@ size_t ag_smem_bytes() { return SMEM_ALLOC; }
 
 int ag_max_pairs()
 {
-    static int cached[64] = {};
+    static std::atomic<int> cached[64] = {};  // per device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cached[dev] > 0) return cached[dev];
+    if (const int c = cached[dev].load(); c > 0) return c;
     if (!set_smem_attr()) return 0;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;

@@ -28,6 +28,8 @@
 //               (S = ((0 + P_0) + P_1) + ...); then rounds S to bf16, stores
 //               the rows to rank j = row / (M/R) with TMA, and publishes the
 //               128x128 output tiles' flags.
+#include <atomic>
+
 #include "opw_device.cuh"
 #include "opw_kernels.h"
 
@@ -357,10 +359,10 @@ size_t rs_smem_bytes() { return SMEM_ALLOC; }
 // Clusters of this kernel that can be resident at once (0 on error).
 int rs_max_pairs()
 {
-    static int cached[64] = {};
+    static std::atomic<int> cached[64] = {};  // per device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cached[dev] > 0) return cached[dev];
+    if (const int c = cached[dev].load(); c > 0) return c;
     if (cudaFuncSetAttribute(gemm_rs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_ALLOC) != cudaSuccess)
         return 0;
@@ -385,7 +387,7 @@ int rs_max_pairs()
 
 cudaError_t launch_gemm_rs(const RsParams& p, int pairs, cudaStream_t s)
 {
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64] = {};  // per device; set once, benign repeats
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
