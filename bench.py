@@ -346,6 +346,31 @@ def alltoall_results(api, torch, reps, R=8, B=8 << 20):
             "hbm_frac": gbs / float(peaks["hbm_gbs"])}
 
 
+def ag_fused_results(api, torch, name, reps):
+    """Fused AG-GEMM launches of one layer alone (its skew schedule included)."""
+    from overlap_producer_warps_gb300 import inputs
+    cfg = inputs.CONFIGS[name]
+    d = inputs.ag_inputs(cfg, seed=0)
+    R, M_r, K, N = cfg["R"], cfg["M_r"], cfg["K"], cfg["N"]
+    dev = torch.device("cuda")
+    heap = torch.from_numpy(d["heap"]).to(dev)
+    B = torch.from_numpy(d["B"].view(np.int16)).to(dev).view(torch.bfloat16)
+    G = torch.empty((R * M_r, K), dtype=torch.bfloat16, device=dev)
+    C = torch.empty((R * M_r, N), dtype=torch.bfloat16, device=dev)
+    sig = api.Signal(api.ag_num_flags(R, M_r, K))
+    kw = {}
+    if cfg.get("skew"):
+        perm, delay = inputs.skew_schedule(0, R)
+        kw = dict(publish_perm=perm, delay_ns=delay)
+    t = time_launches(torch, lambda: api.ag_gemm(heap, d["rank_off"], d["a_off"], M_r, N, K, B, G, C,
+                                                 sig, sig.next_epoch(), api.make_opts(**kw)), reps)
+    st = sig.status()
+    if st[0] != api.OK:
+        raise RuntimeError(f"{name}: device error {st}")
+    sig.close()
+    return {"ms": t, "tflops": flops_ag(cfg) / t / 1e9}
+
+
 def per_config_results(api, torch, peak_tflops, reps=5):
     """Each of the pages' tensor-parallel configurations on its own: fused
     TFLOP/s, the unfused copy-then-GEMM baseline, cuBLAS on the pre-gathered
@@ -669,7 +694,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--prewarm-s", type=float, default=2.0,
                     help="seconds of untimed steps before the warm-up steps (clock ramp)")
-    ap.add_argument("--only", choices=["ring_allreduce", "alltoall"], default=None,
+    ap.add_argument("--only", choices=["ring_allreduce", "alltoall", "ag_tp", "ag_mlp", "ag_skew"],
+                    default=None,
                     help="run only this per-configuration measurement (for profiling) and "
                          "print its result as one JSON line")
     args = ap.parse_args()
@@ -684,8 +710,13 @@ def main():
     if args.only is not None:
         import torch
         from overlap_producer_warps_gb300 import api
-        fn = ring_results if args.only == "ring_allreduce" else alltoall_results
-        print(json.dumps({args.only: fn(api, torch, args.steps)}), flush=True)
+        if args.only == "ring_allreduce":
+            res = ring_results(api, torch, args.steps)
+        elif args.only == "alltoall":
+            res = alltoall_results(api, torch, args.steps)
+        else:
+            res = ag_fused_results(api, torch, args.only, args.steps)
+        print(json.dumps({args.only: res}), flush=True)
         return 0
     if world > 1:
         import torch
