@@ -346,8 +346,9 @@ def alltoall_results(api, torch, reps, R=8, B=8 << 20):
             "hbm_frac": gbs / float(peaks["hbm_gbs"])}
 
 
-def ag_fused_results(api, torch, name, reps):
-    """Fused AG-GEMM launches of one layer alone (its skew schedule included)."""
+def ag_fused_results(api, torch, name, reps, producer_only=False):
+    """Fused AG-GEMM launches of one layer alone (its skew schedule included),
+    or, with producer_only, its gather leg alone (GB/s of shard read + G write)."""
     from overlap_producer_warps_gb300 import inputs
     cfg = inputs.CONFIGS[name]
     d = inputs.ag_inputs(cfg, seed=0)
@@ -362,12 +363,16 @@ def ag_fused_results(api, torch, name, reps):
     if cfg.get("skew"):
         perm, delay = inputs.skew_schedule(0, R)
         kw = dict(publish_perm=perm, delay_ns=delay)
+    if producer_only:
+        kw["role"] = api.ROLE_PRODUCER
     t = time_launches(torch, lambda: api.ag_gemm(heap, d["rank_off"], d["a_off"], M_r, N, K, B, G, C,
                                                  sig, sig.next_epoch(), api.make_opts(**kw)), reps)
     st = sig.status()
     if st[0] != api.OK:
         raise RuntimeError(f"{name}: device error {st}")
     sig.close()
+    if producer_only:
+        return {"ms": t, "gather_hbm_gbs": 2.0 * R * M_r * K * 2 / (t * 1e-3) / 1e9}
     return {"ms": t, "tflops": flops_ag(cfg) / t / 1e9}
 
 
@@ -694,7 +699,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--prewarm-s", type=float, default=2.0,
                     help="seconds of untimed steps before the warm-up steps (clock ramp)")
-    ap.add_argument("--only", choices=["ring_allreduce", "alltoall", "ag_tp", "ag_mlp", "ag_skew"],
+    ap.add_argument("--only", choices=["ring_allreduce", "alltoall", "ag_tp", "ag_mlp", "ag_skew",
+                                       "ag_tp_gather", "ag_mlp_gather", "ag_skew_gather"],
                     default=None,
                     help="run only this per-configuration measurement (for profiling) and "
                          "print its result as one JSON line")
@@ -714,6 +720,9 @@ def main():
             res = ring_results(api, torch, args.steps)
         elif args.only == "alltoall":
             res = alltoall_results(api, torch, args.steps)
+        elif args.only.endswith("_gather"):
+            res = ag_fused_results(api, torch, args.only[:-len("_gather")], args.steps,
+                                   producer_only=True)
         else:
             res = ag_fused_results(api, torch, args.only, args.steps)
         print(json.dumps({args.only: res}), flush=True)
