@@ -144,7 +144,10 @@ typedef struct {
                                 count of this epoch's window), so each slot is
                                 published exactly once per epoch; otherwise the
                                 launch stops with OPW_ERR_FLAG_PROTOCOL (rank, slot).
-                                AG-GEMM and GEMM-RS. */
+                                AG-GEMM and GEMM-RS.  Every launch on the signal
+                                object since its last reset must have covered the
+                                same slots (same R and tile geometry): slots an
+                                earlier launch did not publish hold older epochs. */
 
 #define OPW_SCHED_READY   0  /* dynamic (default): CTAs claim output tiles from a
                                 device counter in the order their rows are
