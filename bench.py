@@ -279,14 +279,18 @@ class TpLayer:
 
 def time_launches(torch, fn, n, warm=2):
     """Mean device time (ms) per launch over n back-to-back launches of fn(),
-    timed with events on the current stream (the host enqueues ahead of the
-    GPU, so host-side launch cost stays out of the interval)."""
+    timed with events on the current stream.  A short spin kernel ahead of
+    the first event keeps the GPU busy while the host enqueues the launches,
+    so neither the first launch's host-side cost nor its launch latency
+    falls inside the interval."""
     s = torch.cuda.current_stream()
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    # about 0.3 ms + 0.1 ms per launch at 2 GHz: more than the host needs
+    torch.cuda._sleep(int(2e9 * (3e-4 + 1e-4 * n)))
     e0.record(s)
     for _ in range(n):
         fn()
@@ -412,6 +416,8 @@ def per_config_results(api, torch, peak_tflops, reps=5):
 
         t_fused = time_launches(torch, fused, reps)
         t_swz = time_launches(torch, lambda: fused(schedule=api.SCHED_SWIZZLE), reps)
+        # every consumer waits for the whole gather before its first tile
+        t_serial = time_launches(torch, lambda: fused(sync_mode=api.SYNC_SERIAL), reps)
         sig_add = api.Signal(api.ag_num_row_counters(R, M_r, K))
 
         def fused_row_add():
@@ -446,10 +452,12 @@ def per_config_results(api, torch, peak_tflops, reps=5):
         out[name] = {
             "fused_tflops": fl / t_fused / 1e9, "pct_of_peak": fl / t_fused / 1e9 / peak_tflops,
             "swizzle_schedule_tflops": fl / t_swz / 1e9,
+            "serial_sync_tflops": fl / t_serial / 1e9,
             "row_add_signal_tflops": fl / t_add / 1e9,
             "unfused_copy_then_gemm_tflops": fl / t_unf / 1e9,
             "cublas_gemm_only_tflops": fl / t_gemm / 1e9,
-            "ms": {"fused": t_fused, "swizzle": t_swz, "row_add": t_add, "producer_only": t_prod,
+            "ms": {"fused": t_fused, "swizzle": t_swz, "serial": t_serial, "row_add": t_add,
+                   "producer_only": t_prod,
                    "consumer_only": t_cons, "unfused": t_unf, "gemm_only": t_gemm},
             "overlap_efficiency": max(0.0, min(1.0, e)),
             "gather_hbm_gbs_producer_only": 2.0 * M * K * 2 / (t_prod * 1e-3) / 1e9,
@@ -487,13 +495,21 @@ def per_config_results(api, torch, peak_tflops, reps=5):
             outs[j].copy_(S[j * (M // R):(j + 1) * (M // R)])
 
     t_unf = time_launches(torch, unfused_rs, reps)
+    # The same FLOPs as one cuBLAS GEMM with the ranks' K slices side by side
+    # ([M, R*K_r] @ [R*K_r, N]): no per-rank partials, no reduction, no scatter.
+    A_cat = torch.cat(A, dim=1)
+    B_cat = torch.cat(Bs, dim=0)
+    C_cat = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    t_gemm = time_launches(torch, lambda: torch.matmul(A_cat, B_cat, out=C_cat), reps)
+    del A_cat, B_cat, C_cat
     st = sig.status()
     if st[0] != api.OK:
         raise RuntimeError(f"rs_tp: device error {st}")
     fl = flops_rs(cfg)
     out["rs_tp"] = {"fused_tflops": fl / t_fused / 1e9, "pct_of_peak": fl / t_fused / 1e9 / peak_tflops,
                     "unfused_partials_then_sum_tflops": fl / t_unf / 1e9,
-                    "ms": {"fused": t_fused, "unfused": t_unf},
+                    "cublas_single_gemm_tflops": fl / t_gemm / 1e9,
+                    "ms": {"fused": t_fused, "unfused": t_unf, "gemm_only": t_gemm},
                     "scatter_hbm_gbs": M * N * 2 / (t_fused * 1e-3) / 1e9}
     sig.close()
     return out
