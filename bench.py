@@ -380,6 +380,28 @@ def ag_fused_results(api, torch, name, reps, producer_only=False):
     return {"ms": t, "tflops": flops_ag(cfg) / t / 1e9}
 
 
+def rs_results(api, torch, reps, scatter_only=False):
+    """GEMM-RS TP launches alone, or, with scatter_only, its scatter leg alone
+    (GB/s of bf16 output stored into the ranks' blocks)."""
+    from overlap_producer_warps_gb300 import inputs
+    cfg = inputs.CONFIGS["rs_tp"]
+    d = inputs.rs_inputs(cfg, seed=0)
+    R, M, K_r, N = cfg["R"], cfg["M"], cfg["K_r"], cfg["N"]
+    heap = torch.from_numpy(d["heap"]).cuda()
+    sig = api.Signal(api.rs_num_flags(R, M, N))
+    role = api.ROLE_CONSUMER if scatter_only else api.ROLE_FUSED
+    t = time_launches(torch, lambda: api.gemm_rs(heap, d["rank_off"], d["a_off"], d["b_off"],
+                                                 d["out_off"], M, N, K_r, sig, sig.next_epoch(),
+                                                 api.make_opts(role=role)), reps)
+    st = sig.status()
+    if st[0] != api.OK:
+        raise RuntimeError(f"rs_tp: device error {st}")
+    sig.close()
+    if scatter_only:
+        return {"ms": t, "scatter_hbm_gbs": M * N * 2 / (t * 1e-3) / 1e9}
+    return {"ms": t, "tflops": flops_rs(cfg) / t / 1e9}
+
+
 def per_config_results(api, torch, peak_tflops, reps=5):
     """Each of the pages' tensor-parallel configurations on its own: fused
     TFLOP/s, the unfused copy-then-GEMM baseline, cuBLAS on the pre-gathered
@@ -477,9 +499,14 @@ def per_config_results(api, torch, peak_tflops, reps=5):
     R, M, K_r, N = cfg["R"], cfg["M"], cfg["K_r"], cfg["N"]
     heap = torch.from_numpy(d["heap"]).cuda()
     sig = api.Signal(api.rs_num_flags(R, M, N))
-    t_fused = time_launches(torch, lambda: api.gemm_rs(heap, d["rank_off"], d["a_off"], d["b_off"],
-                                                       d["out_off"], M, N, K_r, sig,
-                                                       sig.next_epoch()), reps)
+
+    def rs(role=api.ROLE_FUSED):
+        api.gemm_rs(heap, d["rank_off"], d["a_off"], d["b_off"], d["out_off"], M, N, K_r, sig,
+                    sig.next_epoch(), api.make_opts(role=role))
+
+    t_fused = time_launches(torch, rs, reps)
+    t_gemm_leg = time_launches(torch, lambda: rs(api.ROLE_PRODUCER), reps)
+    t_scatter_leg = time_launches(torch, lambda: rs(api.ROLE_CONSUMER), reps)
     A = [heap[int(d["rank_off"][r]) + d["a_off"]:int(d["rank_off"][r]) + d["a_off"] + M * K_r * 2]
          .view(torch.bfloat16).view(M, K_r) for r in range(R)]
     Bs = [heap[int(d["rank_off"][r]) + d["b_off"]:int(d["rank_off"][r]) + d["b_off"] + K_r * N * 2]
@@ -506,11 +533,15 @@ def per_config_results(api, torch, peak_tflops, reps=5):
     if st[0] != api.OK:
         raise RuntimeError(f"rs_tp: device error {st}")
     fl = flops_rs(cfg)
+    e = (t_gemm_leg + t_scatter_leg - t_fused) / min(t_gemm_leg, t_scatter_leg)
     out["rs_tp"] = {"fused_tflops": fl / t_fused / 1e9, "pct_of_peak": fl / t_fused / 1e9 / peak_tflops,
                     "unfused_partials_then_sum_tflops": fl / t_unf / 1e9,
                     "cublas_single_gemm_tflops": fl / t_gemm / 1e9,
-                    "ms": {"fused": t_fused, "unfused": t_unf, "gemm_only": t_gemm},
-                    "scatter_hbm_gbs": M * N * 2 / (t_fused * 1e-3) / 1e9}
+                    "ms": {"fused": t_fused, "gemm_leg_only": t_gemm_leg,
+                           "scatter_leg_only": t_scatter_leg, "unfused": t_unf,
+                           "gemm_only": t_gemm},
+                    "overlap_efficiency": max(0.0, min(1.0, e)),
+                    "scatter_hbm_gbs_scatter_only": M * N * 2 / (t_scatter_leg * 1e-3) / 1e9}
     sig.close()
     return out
 
@@ -716,7 +747,8 @@ def main():
     ap.add_argument("--prewarm-s", type=float, default=2.0,
                     help="seconds of untimed steps before the warm-up steps (clock ramp)")
     ap.add_argument("--only", choices=["ring_allreduce", "alltoall", "ag_tp", "ag_mlp", "ag_skew",
-                                       "ag_tp_gather", "ag_mlp_gather", "ag_skew_gather"],
+                                       "ag_tp_gather", "ag_mlp_gather", "ag_skew_gather",
+                                       "rs_tp", "rs_tp_scatter"],
                     default=None,
                     help="run only this per-configuration measurement (for profiling) and "
                          "print its result as one JSON line")
@@ -736,6 +768,8 @@ def main():
             res = ring_results(api, torch, args.steps)
         elif args.only == "alltoall":
             res = alltoall_results(api, torch, args.steps)
+        elif args.only.startswith("rs_"):
+            res = rs_results(api, torch, args.steps, scatter_only=args.only.endswith("_scatter"))
         elif args.only.endswith("_gather"):
             res = ag_fused_results(api, torch, args.only[:-len("_gather")], args.steps,
                                    producer_only=True)

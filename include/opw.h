@@ -343,9 +343,21 @@ int64_t opw_rs_num_flags(int32_t R, int64_t M, int64_t N);
  * block to its rank, and publish flags[slot] = epoch (.gpu release) per
  * 128x128 output tile.
  *
- * Shapes: M a multiple of 128*R; K_r a multiple of 64; N a multiple of 8.
+ * Roles (opts->role), for timing the two legs apart:
+ *   OPW_ROLE_FUSED    the whole path (default).
+ *   OPW_ROLE_PRODUCER the GEMM leg alone: loads, MMAs and the rank-order
+ *                     sums; no output is stored, no flag is published, and
+ *                     `epoch` (which must still be the next epoch) is not
+ *                     used up.
+ *   OPW_ROLE_CONSUMER the scatter leg alone: no loads and no MMAs, so S is 0;
+ *                     every output tile is stored as bf16 zeros in its
+ *                     rank's block and its flag published with `epoch`.
+ *
+ * Shapes: M a multiple of 128*R; K_r and N multiples of 8 (a ragged last
+ * k-block or column tile is zero-filled by TMA and not stored).
  * Alignment and errors as for opw_ag_gemm.  `opts` fields used: timeout_ns,
- * num_ctas (others must be defaults).
+ * num_ctas, role, sync_mode (OVERLAP or CHECKED); the others must be
+ * defaults.
  */
 opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t out_off,
                        int64_t M, int64_t N, int64_t K_r, opw_signal* sig, uint64_t epoch,

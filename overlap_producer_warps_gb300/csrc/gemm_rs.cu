@@ -28,6 +28,10 @@
 //               (S = ((0 + P_0) + P_1) + ...); then rounds S to bf16, stores
 //               the rows to rank j = row / (M/R) with TMA, and publishes the
 //               128x128 output tiles' flags.
+// For overlap timing the two legs also run alone: OPW_ROLE_PRODUCER runs the
+// GEMM leg (loads, MMAs, the rank-order sums in registers) and stores and
+// publishes nothing; OPW_ROLE_CONSUMER runs the scatter leg alone (no loads,
+// no MMAs: S stays 0, so every output tile is stored as zeros and published).
 #include <atomic>
 
 #include "opw_device.cuh"
@@ -117,6 +121,7 @@ __device__ __forceinline__ PairSched pair_sched(const RsParams& p)
 __device__ void rs_loader(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, const ErrCtx& ec,
                           uint32_t crank)
 {
+    if (p.role == OPW_ROLE_CONSUMER) return;
     const uint32_t lane = lane_id();
     const PairSched ps = pair_sched(p);
     const int KB = (p.K_r + BK - 1) / BK;
@@ -157,6 +162,7 @@ __device__ void rs_loader(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, const 
 __device__ void rs_mma(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32_t tmem,
                        const ErrCtx& ec)
 {
+    if (p.role == OPW_ROLE_CONSUMER) return;
     const uint32_t lane = lane_id();
     const PairSched ps = pair_sched(p);
     const int KB = (p.K_r + BK - 1) / BK;
@@ -211,6 +217,8 @@ __device__ void rs_reduce(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32
     uint32_t empty_caddr[2];
     for (int a = 0; a < 2; ++a) empty_caddr[a] = mapa_shared(smem_u32(&ctrl->tmem_empty[a]), 0);
     uint32_t acc = 0, aphase = 0;
+    const bool reduce = p.role != OPW_ROLE_CONSUMER;
+    const bool scatter = p.role != OPW_ROLE_PRODUCER;
     for (int i = 0; i < ps.nt; ++i) {
         bool ok = true;
         const int q = ps.cid + i * ps.nc;
@@ -220,7 +228,7 @@ __device__ void rs_reduce(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32
 #pragma unroll
         for (int e = 0; e < 128; ++e) S[e] = 0.0f;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        for (int r = 0; r < p.R; ++r) {
+        for (int r = 0; r < p.R && reduce; ++r) {
             if (!wait_bar(&ctrl->tmem_full[acc], aphase, ec, SITE_EPI_TMEM_FULL)) { ok = false; break; }
             tc_fence_after();
             const uint32_t taddr = tmem + lane_off + acc * BN + half * 128;
@@ -241,7 +249,7 @@ __device__ void rs_reduce(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32
         // Scatter: these rows belong to rank j; store them in its slice.  In a
         // ragged last pair tile the odd CTA's rows may lie past M: it reduced
         // zeros and stores nothing.
-        const bool rows_in = m0 < p.M;
+        const bool rows_in = scatter && m0 < p.M;
         const int j = rows_in ? m0 / p.Mb : 0;
         const int row_in_block = m0 - j * p.Mb + quarter * 32;
 #pragma unroll

@@ -445,7 +445,8 @@ opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t 
     opw_opts tmp;
     const opw_opts& o = opts_or_default(opts_in, tmp);
     if ((o.sync_mode != OPW_SYNC_OVERLAP && o.sync_mode != OPW_SYNC_CHECKED) || o.schedule != 0 ||
-        o.role != 0 || o.publish_perm != nullptr || o.delay_ns != nullptr || o.fault_kind != 0 ||
+        o.role < OPW_ROLE_FUSED || o.role > OPW_ROLE_CONSUMER || o.publish_perm != nullptr ||
+        o.delay_ns != nullptr || o.fault_kind != 0 ||
         o.num_ctas < 0 || o.signal_mode != 0 || o.local_rank < -1 || o.local_rank > 0)
         return OPW_ERR_INVALID_ARG;
     const int R = symm->R;
@@ -499,9 +500,11 @@ opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t 
     p.T_fm = static_cast<int32_t>(Mb / 128);
     p.T_fn = static_cast<int32_t>((N + 127) / 128);
     p.checked = o.sync_mode == OPW_SYNC_CHECKED;
+    p.role = o.role;
     if (launch_gemm_rs(p, pairs, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return OPW_ERR_CUDA;
-    sig->epoch_last = epoch;
+    // The GEMM leg alone publishes nothing: the epoch stays the next one.
+    if (o.role != OPW_ROLE_PRODUCER) sig->epoch_last = epoch;
     return OPW_OK;
 }
 

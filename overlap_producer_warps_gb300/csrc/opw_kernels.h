@@ -88,6 +88,7 @@ struct RsParams {
     int32_t T_M, T_N;         // 256 x 256 pair tiles along M, along N
     int32_t T_fm, T_fn;       // 128x128 flag tiles per rank block along M, along N
     int32_t checked;          // OPW_SYNC_CHECKED: publish by exchange, expect epoch-1
+    int32_t role;             // OPW_ROLE_*: FUSED, PRODUCER (GEMM leg), CONSUMER (scatter leg)
 };
 
 struct RingParams {

@@ -187,6 +187,9 @@ def test_gemm_rs_rejects_bad_arguments_on_the_host(api):
     assert rs(K_r=4) == E.ERR_UNSUPPORTED_SHAPE
     assert rs(b_off=8) == E.ERR_MISALIGNED
     assert rs(opts=api.make_opts(publish_perm=[1, 0])) == E.ERR_INVALID_ARG
+    assert rs(opts=api.make_opts(role=3)) == E.ERR_INVALID_ARG
+    assert rs(opts=api.make_opts(role=-1)) == E.ERR_INVALID_ARG
+    assert rs(opts=api.make_opts(sync_mode=api.SYNC_SERIAL)) == E.ERR_INVALID_ARG
     assert rs() == E.ERR_INVALID_ARG                    # too few slots
 
 

@@ -62,6 +62,45 @@ def test_shapes(api, R, M, K_r, N, order):
     _check_all(api, prob)
 
 
+def test_legs_alone(api):
+    """The GEMM leg alone (producer role) stores and publishes nothing and
+    leaves the epoch unused; the scatter leg alone (consumer role) stores
+    bf16 zeros into every rank's block and publishes every flag; a fused
+    launch after both gives the oracle's result."""
+    R, M, K_r, N = 3, 768, 192, 328   # ragged last column tile
+    d = inputs.rs_inputs(_cfg(R, M, K_r, N), seed=53)
+    prob = RsProblem(d)
+    F = api.rs_num_flags(R, M, N)
+    sig = api.Signal(F)
+    out_bytes = prob.Mb * N * 2
+    regions = [prob.heap[int(prob.rank_off[j]) + d["out_off"]:
+                         int(prob.rank_off[j]) + d["out_off"] + out_bytes] for j in range(R)]
+    for reg in regions:
+        reg.fill_(0x7F)
+    e = sig.next_epoch()
+    prob.run(api, sig, e, api.make_opts(role=api.ROLE_PRODUCER))
+    torch.cuda.synchronize()
+    assert sig.status()[0] == api.OK
+    assert sig.next_epoch() == e
+    assert not sig.flags().any()
+    for reg in regions:
+        assert bool((reg == 0x7F).all())
+
+    prob.run(api, sig, e, api.make_opts(role=api.ROLE_CONSUMER))
+    torch.cuda.synchronize()
+    assert sig.status()[0] == api.OK
+    assert np.array_equal(sig.flags().cpu().numpy(), oracle.expected_flags(F, e))
+    for reg in regions:
+        assert not bool(reg.any())
+
+    e2 = sig.next_epoch()
+    assert e2 == e + 1
+    prob.run(api, sig, e2, api.make_opts(sync_mode=api.SYNC_CHECKED))
+    assert sig.status()[0] == api.OK
+    assert np.array_equal(sig.flags().cpu().numpy(), oracle.expected_flags(F, e2))
+    _check_all(api, prob)
+
+
 @pytest.mark.parametrize("num_ctas", [1, 2, 5, 6])
 def test_pair_counts(api, num_ctas):
     """CTAs run in pairs: 1 and 2 CTAs give one pair, 5 gives two.  With 15
