@@ -28,7 +28,8 @@
 //              (none for the local rank's rows, which are read in place), and
 //              only then puts it on both CTAs' tile queues.  Acquiring ahead
 //              of the loaders keeps every global-memory round trip off the
-//              k-block loop.
+//              k-block loop.  In the odd CTA it forwards the release of each
+//              queue slot to the even CTA (see pop_tile).
 // The GPU plays the consumer of rank p.local_rank (or none, -1): that rank's
 // shard is local, so its tiles are taken first and its own flags are never
 // waited for; its producer copies still fill G, after every other rank's.
@@ -60,7 +61,8 @@ struct AgCtrl {
     uint64_t tmem_empty[2];     // even CTA: both CTAs' epilogues have read it
     uint64_t gfull[GATHER_BUFS];
     uint64_t tq_full[TILE_Q];   // each CTA: a tile id is in its queue slot
-    uint64_t tq_empty[TILE_Q];  // even CTA: every reader of the slot, in both CTAs, is done
+    uint64_t tq_empty[TILE_Q];  // even CTA: its readers of the slot and the odd CTA's forwarder are done
+    uint64_t tq_fwd[TILE_Q];    // odd CTA: its readers of the slot are done
     uint64_t need_next;         // even CTA, loader -> scheduler: claim the next tile now
     uint64_t mma_done;
     int32_t tile_q[TILE_Q];
@@ -85,9 +87,12 @@ static_assert(OFF_B % 1024 == 0 && OFF_EPI % 1024 == 0 && OFF_GATHER % 1024 == 0
 // acquire and the first TMA loads.
 constexpr int CLAIM_LEAD_KB = 64;
 
-// Readers of each tile-queue slot: loader, MMA and 4 epilogue warps of the
-// even CTA, loader and 4 epilogue warps of the odd one.
-constexpr uint32_t TQ_READERS = 1 + 1 + 4 + 1 + 4;
+// Arrivals that free a tile-queue slot on the even CTA's tq_empty: its
+// loader, MMA and 4 epilogue warps, and the odd CTA's forwarder, which
+// arrives once the odd CTA's readers (loader and 4 epilogue warps) have all
+// arrived on its tq_fwd.
+constexpr uint32_t TQ_READERS = 1 + 1 + 4 + 1;
+constexpr uint32_t TQ_ODD_READERS = 1 + 4;
 
 constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators of 256 columns
 constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, /*B MN-major*/ true);
@@ -326,18 +331,43 @@ __device__ __forceinline__ bool issue_kblocks(const AgParams& p, uint8_t* smem, 
     return true;
 }
 
-// Take the next tile id from this CTA's queue and release the slot on the
-// even CTA's tq_empty (-2 when the wait failed).
+// Take the next tile id from this CTA's queue and release the slot (-2 when
+// the wait failed).  The release is a local arrive with CTA-scope release
+// semantics: on the even CTA's tq_empty, or on the odd CTA's tq_fwd, from
+// which the odd CTA's warp 3 forwards it (run_forwarder).  A cluster-scope
+// release arrive here cost about 1000 cycles per pop, and the loader and MMA
+// threads pop at every tile boundary.
 __device__ __forceinline__ int pop_tile(AgCtrl* ctrl, const ErrCtx& ec, uint32_t& tq,
-                                        uint32_t& tqphase)
+                                        uint32_t& tqphase, uint32_t crank)
 {
     if (!wait_bar_cluster(&ctrl->tq_full[tq], tqphase, ec, SITE_TILE_QUEUE)) return -2;
     const int q = reinterpret_cast<volatile int32_t*>(ctrl->tile_q)[tq];
     __syncwarp();
-    if (lane_id() == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctrl->tq_empty[tq]), 0));
+    if (lane_id() == 0) mbar_arrive(crank == 0 ? &ctrl->tq_empty[tq] : &ctrl->tq_fwd[tq]);
     __syncwarp();
     if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
     return q;
+}
+
+// Odd CTA, warp 3: for each queue slot in turn, wait until the odd CTA's
+// readers have taken it (tq_fwd), then free it on the even CTA's tq_empty
+// with one cluster-scope release arrive.  That release is cumulative: it
+// carries the readers' CTA-scope releases, so their reads of the slot come
+// before the scheduler overwrites it.  Stops after the end-of-work entry.
+__device__ void run_forwarder(AgCtrl* ctrl, const ErrCtx& ec)
+{
+    const uint32_t empty0 = mapa_shared(smem_u32(&ctrl->tq_empty[0]), 0);
+    uint32_t tq = 0, tqphase = 0;
+    while (true) {
+        if (!wait_bar_cluster(&ctrl->tq_full[tq], tqphase, ec, SITE_TILE_QUEUE)) return;
+        const int q = reinterpret_cast<volatile int32_t*>(ctrl->tile_q)[tq];
+        if (!wait_bar(&ctrl->tq_fwd[tq], tqphase, ec, SITE_TILE_QUEUE)) return;
+        __syncwarp();
+        if (lane_id() == 0) mbar_arrive_cluster(empty0 + 8u * tq);
+        __syncwarp();
+        if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
+        if (q < 0) return;
+    }
 }
 
 // Even CTA, warp 3.
@@ -429,7 +459,7 @@ __device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
     LoaderRing rg;
     uint32_t tq = 0, tqphase = 0;
     while (true) {
-        const int q = pop_tile(ctrl, ec, tq, tqphase);
+        const int q = pop_tile(ctrl, ec, tq, tqphase, crank);
         if (q < 0) break;
         // consume_token: the scheduler's flag acquires reach this thread
         // through the queue barrier; order them before the async-proxy
@@ -466,7 +496,7 @@ __device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t
     uint32_t stage = 0, sphase = 0, acc = 0, aphase = 0, tq = 0, tqphase = 0;
     bool ok = true;
     while (ok) {
-        const int q = pop_tile(ctrl, ec, tq, tqphase);
+        const int q = pop_tile(ctrl, ec, tq, tqphase, 0u);
         if (q < 0) break;
 
         // both CTAs' epilogues have read this accumulator
@@ -519,7 +549,7 @@ __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uin
     const uint32_t empty_caddr0 = mapa_shared(smem_u32(&ctrl->tmem_empty[0]), 0);
     uint32_t acc = 0, aphase = 0, tq = 0, tqphase = 0;
     while (true) {
-        const int q = pop_tile(ctrl, ec, tq, tqphase);
+        const int q = pop_tile(ctrl, ec, tq, tqphase, crank);
         if (q < 0) break;
 
         const int m0 = (q / p.T_N) * PAIR_M + static_cast<int>(crank) * BM;
@@ -761,6 +791,7 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
         for (int i = 0; i < TILE_Q; ++i) {
             mbar_init(&ctrl->tq_full[i], 1);
             mbar_init(&ctrl->tq_empty[i], TQ_READERS);
+            mbar_init(&ctrl->tq_fwd[i], TQ_ODD_READERS);
         }
         mbar_init(&ctrl->need_next, 1);
         mbar_init(&ctrl->mma_done, 1);
@@ -803,6 +834,7 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
             if (producer) run_gather(p, smem, ctrl, ec, t_start);
         } else if (warp == 3) {
             if (consumer && crank == 0) run_scheduler(p, ctrl, ec);
+            if (consumer && crank == 1) run_forwarder(ctrl, ec);
         } else {
             if (consumer) run_epilogue(p, smem, ctrl, tmem, ec, warp, crank);
         }
