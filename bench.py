@@ -290,7 +290,9 @@ def time_launches(torch, fn, n, warm=2):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     # about 0.3 ms + 0.1 ms per launch at 2 GHz: more than the host needs
-    torch.cuda._sleep(int(2e9 * (3e-4 + 1e-4 * n)))
+    spin = getattr(torch.cuda, "_sleep", None)
+    if spin is not None:
+        spin(int(2e9 * (3e-4 + 1e-4 * n)))
     e0.record(s)
     for _ in range(n):
         fn()
