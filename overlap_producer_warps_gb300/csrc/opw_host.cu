@@ -481,7 +481,7 @@ opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t 
     for (int r = 0; r < R; ++r) {
         char* base = heap + symm->rank_off[r];
         if (!make_map(&p.a_load[r], base + a_off, K_r, M, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !make_map(&p.b_load[r], base + b_off, N, K_r, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map(&p.b_load[r], base + b_off, N, K_r, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !make_map(&p.out_store[r], base + out_off, N, Mb, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
             return OPW_ERR_CUDA;
     }

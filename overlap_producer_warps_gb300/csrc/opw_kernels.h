@@ -77,7 +77,7 @@ struct AgParams {
 
 struct RsParams {
     CUtensorMap a_load[OPW_MAX_RANKS];  // A_r [M, K_r], box {64, 128}, 128B swizzle
-    CUtensorMap b_load[OPW_MAX_RANKS];  // B_r [K_r, N], box {64, 64}, 128B swizzle
+    CUtensorMap b_load[OPW_MAX_RANKS];  // B_r [K_r, N], box {64, 128}, 128B swizzle
     CUtensorMap out_store[OPW_MAX_RANKS];  // out_j [M/R, N], box {64, 32}, 128B swizzle
     int64_t* flags;
     int32_t* status;
