@@ -48,6 +48,8 @@ def _check_all(api, prob, rows=None):
     (8, 1024, 64, 512, None),
     (1, 256, 320, 264, None),          # single rank: plain GEMM
     (4, 1024, 448, 1024, (3, 1, 2, 0)),
+    (2, 256, 8, 256, None),            # K_r = 8: one k-stage, almost all of it zero fill
+    (3, 384, 136, 200, None),          # a second k-stage holding 8 of K
 ])
 def test_shapes(api, R, M, K_r, N, order):
     d = inputs.rs_inputs(_cfg(R, M, K_r, N), seed=R * 5 + K_r, slot_order=order)
