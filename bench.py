@@ -142,11 +142,6 @@ def whole_job_tflops(world: int, flops_per_rank_step: float, ms_per_step_max: fl
     return world * flops_per_rank_step / (ms_per_step_max * 1e-3) / 1e12
 
 
-def source_hash(fname: str) -> str:
-    src = os.path.join(ROOT, "overlap_producer_warps_gb300", "csrc", fname)
-    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-
-
 # ------------------------------------------------------------------ CPU oracle sample
 
 def oracle_sample(ag_d, rs_d, ag_cfg, rs_cfg, min_seconds=10.0, max_seconds=30.0, chunk=None):
