@@ -399,6 +399,44 @@ def rs_results(api, torch, reps, scatter_only=False):
     return {"ms": t, "tflops": flops_rs(cfg) / t / 1e9}
 
 
+def tiny_results(api, torch, reps=50):
+    """The tiny AG-GEMM configuration (R=2, 64x128 shards, K=N=128), which is
+    bound by latency: the device time per launch back to back, and the time
+    from the host call to the completed launch (call, then synchronise)."""
+    import time as _time
+    from overlap_producer_warps_gb300 import inputs
+    cfg = inputs.CONFIGS["ag_tiny"]
+    d = inputs.ag_inputs(cfg, seed=0)
+    R, M_r, K, N = cfg["R"], cfg["M_r"], cfg["K"], cfg["N"]
+    heap = torch.from_numpy(d["heap"]).cuda()
+    B = torch.from_numpy(d["B"].view(np.int16)).cuda().view(torch.bfloat16)
+    G = torch.empty((R * M_r, K), dtype=torch.bfloat16, device="cuda")
+    C = torch.empty((R * M_r, N), dtype=torch.bfloat16, device="cuda")
+    sig = api.Signal(api.ag_num_flags(R, M_r, K))
+
+    def run():
+        api.ag_gemm(heap, d["rank_off"], d["a_off"], M_r, N, K, B, G, C, sig, sig.next_epoch())
+
+    t_dev = time_launches(torch, run, reps)
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    lat = []
+    for _ in range(reps):
+        t0 = _time.perf_counter()
+        run()
+        torch.cuda.synchronize()
+        lat.append(_time.perf_counter() - t0)
+    st = sig.status()
+    if st[0] != api.OK:
+        raise RuntimeError(f"ag_tiny: device error {st}")
+    sig.close()
+    lat.sort()
+    return {"us_per_launch_back_to_back": t_dev * 1e3,
+            "us_call_to_done_median": lat[len(lat) // 2] * 1e6,
+            "us_call_to_done_min": lat[0] * 1e6}
+
+
 def per_config_results(api, torch, peak_tflops, reps=5):
     """Each of the pages' tensor-parallel configurations on its own: fused
     TFLOP/s, the unfused copy-then-GEMM baseline, cuBLAS on the pre-gathered
@@ -488,6 +526,7 @@ def per_config_results(api, torch, peak_tflops, reps=5):
         del heap, B, G, C, shards
         torch.cuda.empty_cache()
 
+    out["ag_tiny"] = tiny_results(api, torch)
     out["ring_allreduce"] = ring_results(api, torch, reps)
     out["alltoall"] = alltoall_results(api, torch, reps)
 
@@ -743,7 +782,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--prewarm-s", type=float, default=2.0,
                     help="seconds of untimed steps before the warm-up steps (clock ramp)")
-    ap.add_argument("--only", choices=["ring_allreduce", "alltoall", "ag_tp", "ag_mlp", "ag_skew",
+    ap.add_argument("--only", choices=["ring_allreduce", "alltoall", "ag_tiny", "ag_tp", "ag_mlp", "ag_skew",
                                        "ag_tp_gather", "ag_mlp_gather", "ag_skew_gather",
                                        "rs_tp", "rs_tp_scatter"],
                     default=None,
@@ -765,6 +804,8 @@ def main():
             res = ring_results(api, torch, args.steps)
         elif args.only == "alltoall":
             res = alltoall_results(api, torch, args.steps)
+        elif args.only == "ag_tiny":
+            res = tiny_results(api, torch)
         elif args.only.startswith("rs_"):
             res = rs_results(api, torch, args.steps, scatter_only=args.only.endswith("_scatter"))
         elif args.only.endswith("_gather"):
