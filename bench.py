@@ -144,6 +144,29 @@ def whole_job_tflops(world: int, flops_per_rank_step: float, ms_per_step_max: fl
 
 # ------------------------------------------------------------------ CPU oracle sample
 
+def cpu_model() -> str:
+    """The host CPU's model as /proc/cpuinfo states it (on Arm: implementer
+    and part numbers)."""
+    try:
+        lines = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return "unknown"
+    fields = {}
+    for ln in lines:
+        if ":" in ln:
+            k, v = ln.split(":", 1)
+            fields.setdefault(k.strip().lower(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    if "cpu part" in fields:
+        arm = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1",
+               "0xd49": "Arm Neoverse N2", "0xd0c": "Arm Neoverse N1"}
+        part = fields["cpu part"].lower()
+        name = arm.get(part) if fields.get("cpu implementer", "").lower() == "0x41" else None
+        return name or f"implementer {fields.get('cpu implementer', '?')} part {part}"
+    return "unknown"
+
+
 def oracle_sample(ag_d, rs_d, ag_cfg, rs_cfg, min_seconds=10.0, max_seconds=30.0, chunk=None):
     """Time the oracle on rows of the two outputs until min_seconds have passed."""
     import oracle
@@ -172,6 +195,7 @@ def oracle_sample(ag_d, rs_d, ag_cfg, rs_cfg, min_seconds=10.0, max_seconds=30.0
             break
     el = time.perf_counter() - t0
     return {"value": flops / el / 1e12, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"{rows_ag} rows of the AG-GEMM output (each 4096 columns, K=4096) and "
                       f"{rows_rs} rows of the GEMM-RS output (each 4096 columns, 8 ranks x "
                       f"K_r=1792), fp64, {el:.1f} s"}
@@ -216,7 +240,7 @@ def run_reference(args, rank, world):
             "data": "synthetic", "impl": "reference",
             "config": {"workload": WORKLOAD + " (bounded row sample per step)"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(),
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
