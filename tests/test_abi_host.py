@@ -5,7 +5,6 @@ import ctypes
 import os
 import re
 import subprocess
-import tempfile
 
 import pytest
 import torch
@@ -61,12 +60,12 @@ int main(void) {
   return 0;
 }
 """
-    with tempfile.TemporaryDirectory() as d:
-        c = os.path.join(d, "layout.c")
-        exe = os.path.join(d, "layout")
-        open(c, "w").write(src)
-        subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), c, "-o", exe], check=True)
-        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+    d = os.path.dirname(api.LIB_PATH)  # the library's build folder (not tracked)
+    c = os.path.join(d, "layout.c")
+    exe = os.path.join(d, "layout")
+    open(c, "w").write(src)
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), c, "-o", exe], check=True)
+    out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
     opts = [int(v) for v in out[0].split()]
     symm = [int(v) for v in out[1].split()]
     O, S = api.Opts, api.Symm
