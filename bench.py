@@ -1,11 +1,14 @@
 #!/usr/bin/env python3
 """Benchmark: AG-GEMM / GEMM-RS bf16 TFLOP/s on GB300, and % of dense tensor-core peak.
 
-One step = one pass of the whole hot path over the tensor-parallel layer:
-AllGather->GEMM (R=8 shards of 1024x4096, B 4096x4096) followed by
-GEMM->ReduceScatter (R=8, A_r 8192x1792, B_r 1792x4096), each through the
-C ABI with a fresh epoch.  Inputs (about 656 MiB per step) are larger than
-L2, so no flush is needed between steps.
+One step = one pass of the hot path over the largest configuration, the
+AllGather->GEMM layer with skewed readiness: R=8 logical ranks, each shard
+A_r 4096x8192 bf16, B 8192x8192 bf16, C = concat(A_0..A_7) @ B (32768x8192),
+the ranks published in a seeded permutation with seeded 0-50 us start
+delays.  Every step is one launch through the C ABI with a fresh epoch.
+Inputs (about 1.7 GB per step) are larger than L2, so no flush is needed
+between steps.  The tp_layer step (AG-GEMM TP then GEMM-RS TP) and every
+other configuration are reported in the per_config section.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -25,6 +28,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -35,8 +39,11 @@ if ROOT not in sys.path:
 
 METRIC = "AG-GEMM / GEMM-RS bf16 TFLOP/s on 1 GB300 and % of dense tensor-core peak"
 UNIT = "TFLOP/s"
-WORKLOAD = ("tp_layer: AG-GEMM R=8 A_r 1024x4096 @ B 4096x4096 -> C 8192x4096, then "
-            "GEMM-RS R=8 A_r 8192x1792 @ B_r 1792x4096 -> 8 x (1024x4096)")
+HEADLINE = "ag_skew"
+WORKLOAD = ("ag_skew: AG-GEMM R=8 A_r 4096x8192 @ B 8192x8192 -> C 32768x8192 bf16, ranks "
+            "published in a seeded permutation with seeded 0-50 us start delays")
+TP_WORKLOAD = ("tp_layer: AG-GEMM R=8 A_r 1024x4096 @ B 4096x4096 -> C 8192x4096, then "
+               "GEMM-RS R=8 A_r 8192x1792 @ B_r 1792x4096 -> 8 x (1024x4096)")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -60,53 +67,71 @@ def flops_rs(cfg):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU works."""
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU
+    works.  Each sample is stamped with the host's monotonic clock when it
+    arrives, so a summary can cover one timed window."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, interval_ms: int = 20):
         self.proc = None
         self.dev = device_index
+        self.interval_ms = interval_ms
+        self.samples = []  # (host time, sm MHz, max MHz, power W, set of reasons)
+        self._thread = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", str(self.dev)],
+                 "-lms", str(self.interval_ms), "-i", str(self.dev)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
 
-    def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
+    def _read(self):
+        for line in self.proc.stdout:
+            t = time.monotonic()
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
+                sm, smax, power = float(parts[1]), float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+            reasons = {n for n, v in zip(self.NAMES, parts[5:9]) if v.lower().startswith("active")}
+            self.samples.append((t, sm, smax, power, reasons))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, max clock and power, and the throttle reasons seen,
+        over the samples that arrived in [t0, t1] (all samples if None)."""
+        sel = [x for x in self.samples
+               if (t0 is None or x[0] >= t0) and (t1 is None or x[0] <= t1)]
+        reasons = set()
+        for x in sel:
+            reasons |= x[4]
+        return {"sm_mhz": statistics.median([x[1] for x in sel]) if sel else None,
+                "sm_max_mhz": max(x[2] for x in sel) if sel else None,
+                "power_w_max": max(x[3] for x in sel) if sel else None,
+                "reasons": sorted(reasons), "samples": len(sel)}
 
 
 def kernel_traffic(name: str):
@@ -167,38 +192,33 @@ def cpu_model() -> str:
     return "unknown"
 
 
-def oracle_sample(ag_d, rs_d, ag_cfg, rs_cfg, min_seconds=10.0, max_seconds=30.0, chunk=None):
-    """Time the oracle on rows of the two outputs until min_seconds have passed."""
+def oracle_rows_step(d, rows):
+    """The oracle's rows of C = concat(A_r) @ B for one sample (fp64, all host cores)."""
+    import oracle
+    oracle.ag_gemm_rows(d["heap"], d["rank_off"], d["R"], d["a_off"], d["M_r"], d["N"], d["K"],
+                        d["B"], rows)
+    return 2.0 * len(rows) * d["N"] * d["K"]
+
+
+def oracle_sample(d, min_seconds=10.0, max_seconds=30.0):
+    """Time the oracle on random rows of the headline layer's C until
+    min_seconds have passed."""
     import oracle
     oracle.build()
     rng = np.random.default_rng(7)
-    M_ag = ag_cfg["R"] * ag_cfg["M_r"]
-    flops = 0.0
-    rows_ag = rows_rs = 0
-    t0 = time.perf_counter()
-    step = 0
-    chunk = chunk or max(4, oracle.threads())
+    M = d["R"] * d["M_r"]
+    chunk = max(4, oracle.threads())
+    flops, rows, t0 = 0.0, 0, time.perf_counter()
     while True:
-        ra = rng.integers(0, M_ag, size=chunk)
-        oracle.ag_gemm_rows(ag_d["heap"], ag_d["rank_off"], ag_d["R"], ag_d["a_off"], ag_d["M_r"],
-                            ag_d["N"], ag_d["K"], ag_d["B"], ra)
-        flops += 2.0 * chunk * ag_d["N"] * ag_d["K"]
-        rows_ag += chunk
-        rr = rng.integers(0, rs_d["M"], size=max(1, chunk // 4))
-        oracle.gemm_rs_rows(rs_d["heap"], rs_d["rank_off"], rs_d["R"], rs_d["a_off"],
-                            rs_d["b_off"], rs_d["M"], rs_d["N"], rs_d["K_r"], rr)
-        flops += 2.0 * len(rr) * rs_d["N"] * rs_d["R"] * rs_d["K_r"]
-        rows_rs += len(rr)
-        step += 1
+        flops += oracle_rows_step(d, rng.integers(0, M, size=chunk))
+        rows += chunk
         el = time.perf_counter() - t0
         if el >= min_seconds or el >= max_seconds:
             break
-    el = time.perf_counter() - t0
     return {"value": flops / el / 1e12, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
             "cpu_model": cpu_model(),
-            "sample": f"{rows_ag} rows of the AG-GEMM output (each 4096 columns, K=4096) and "
-                      f"{rows_rs} rows of the GEMM-RS output (each 4096 columns, 8 ranks x "
-                      f"K_r=1792), fp64, {el:.1f} s"}
+            "sample": f"{rows} random rows of the {HEADLINE} layer's C (each {d['N']} columns, "
+                      f"K={d['K']}), fp64, {el:.1f} s"}
 
 
 # ------------------------------------------------------------------ reference arm
@@ -209,31 +229,24 @@ def run_reference(args, rank, world):
     from overlap_producer_warps_gb300 import inputs
     import oracle
     oracle.build()
-    ag_cfg, rs_cfg = inputs.CONFIGS["ag_tp"], inputs.CONFIGS["rs_tp"]
-    ag_d = inputs.ag_inputs(ag_cfg, seed=0)
-    rs_d = inputs.rs_inputs(rs_cfg, seed=0)
+    d = inputs.ag_inputs(inputs.CONFIGS[HEADLINE], seed=0)
     rng = np.random.default_rng(11)
-    n_ag, n_rs = max(4, oracle.threads()), max(2, oracle.threads() // 2)
-    M_ag = ag_cfg["R"] * ag_cfg["M_r"]
+    n_rows = max(4, oracle.threads())
+    M = d["R"] * d["M_r"]
 
     def step():
-        ra = rng.integers(0, M_ag, size=n_ag)
-        oracle.ag_gemm_rows(ag_d["heap"], ag_d["rank_off"], ag_d["R"], ag_d["a_off"], ag_d["M_r"],
-                            ag_d["N"], ag_d["K"], ag_d["B"], ra)
-        rr = rng.integers(0, rs_d["M"], size=n_rs)
-        oracle.gemm_rs_rows(rs_d["heap"], rs_d["rank_off"], rs_d["R"], rs_d["a_off"],
-                            rs_d["b_off"], rs_d["M"], rs_d["N"], rs_d["K_r"], rr)
+        return oracle_rows_step(d, rng.integers(0, M, size=n_rows))
 
-    flops_step = 2.0 * n_ag * ag_d["N"] * ag_d["K"] + 2.0 * n_rs * rs_d["N"] * rs_d["R"] * rs_d["K_r"]
     for _ in range(args.warmup):
         step()
+    flops = 0.0
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step()
+        flops += step()
     el = time.perf_counter() - t0
-    value = flops_step * args.steps / el / 1e12
-    sample = (f"per step: {n_ag} rows of the AG-GEMM output and {n_rs} rows of the GEMM-RS "
-              f"output of the tp_layer workload, fp64 CPU oracle")
+    value = flops / el / 1e12
+    sample = (f"per step: {n_rows} random rows of the {HEADLINE} layer's C (each {d['N']} "
+              f"columns, K={d['K']}), fp64 CPU oracle")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -247,77 +260,127 @@ def run_reference(args, rank, world):
     return 0
 
 
-# ------------------------------------------------------------------ our arm
+# ------------------------------------------------------------------ workloads on the device
 
-class TpLayer:
-    """The tp_layer workload on the device: `sets` copies of every input and
-    output buffer (the end-to-end leg double-buffers them) and one signal
-    object per kernel, shared by the sets since its launches are serial."""
+def skew_opts(api, cfg, **kw):
+    """Options of an AG-GEMM layer: its skew schedule (if any) plus kw."""
+    from overlap_producer_warps_gb300 import inputs
+    if cfg.get("skew"):
+        perm, delay = inputs.skew_schedule(0, cfg["R"])
+        kw = dict(publish_perm=perm, delay_ns=delay, **kw)
+    return api.make_opts(**kw)
 
-    def __init__(self, api, torch, seed=0, sets=1):
+
+class AgLayer:
+    """One AllGather->GEMM configuration on the device: `sets` copies of every
+    input and output buffer (the end-to-end leg double-buffers them) and one
+    signal object, shared by the sets since its launches are serial."""
+
+    def __init__(self, api, torch, name, seed=0, sets=1):
         from overlap_producer_warps_gb300 import inputs
-        self.api, self.torch = api, torch
-        self.ag_cfg, self.rs_cfg = inputs.CONFIGS["ag_tp"], inputs.CONFIGS["rs_tp"]
-        self.ag_d = inputs.ag_inputs(self.ag_cfg, seed=seed)
-        self.rs_d = inputs.rs_inputs(self.rs_cfg, seed=seed)
-        a, r = self.ag_d, self.rs_d
+        self.api, self.torch, self.name = api, torch, name
+        self.cfg = inputs.CONFIGS[name]
+        self.d = inputs.ag_inputs(self.cfg, seed=seed)
+        d = self.d
         dev = torch.device("cuda")
-        M = a["R"] * a["M_r"]
+        self.M = d["R"] * d["M_r"]
         self.bufs = []
         for _ in range(sets):
             self.bufs.append({
-                "ag_heap": torch.from_numpy(a["heap"]).to(dev),
-                "B": torch.from_numpy(a["B"].view(np.int16)).to(dev).view(torch.bfloat16),
-                "G": torch.empty((M, a["K"]), dtype=torch.bfloat16, device=dev),
-                "C": torch.empty((M, a["N"]), dtype=torch.bfloat16, device=dev),
-                "rs_heap": torch.from_numpy(r["heap"]).to(dev),
+                "heap": torch.from_numpy(d["heap"]).to(dev),
+                "B": torch.from_numpy(d["B"].view(np.int16)).to(dev).view(torch.bfloat16),
+                "G": torch.empty((self.M, d["K"]), dtype=torch.bfloat16, device=dev),
+                "C": torch.empty((self.M, d["N"]), dtype=torch.bfloat16, device=dev),
             })
-        self.sig_ag = api.Signal(api.ag_num_flags(a["R"], a["M_r"], a["K"]))
-        self.sig_rs = api.Signal(api.rs_num_flags(r["R"], r["M"], r["N"]))
-        self.flops_ag = flops_ag(self.ag_cfg)
-        self.flops_rs = flops_rs(self.rs_cfg)
+        self.sig = api.Signal(api.ag_num_flags(d["R"], d["M_r"], d["K"]))
+        self.flops = flops_ag(self.cfg)
+        self._opts = {}
 
-    def ag(self, stream=None, b=0):
-        a, d = self.ag_d, self.bufs[b]
-        self.api.ag_gemm(d["ag_heap"], a["rank_off"], a["a_off"], a["M_r"], a["N"], a["K"],
-                         d["B"], d["G"], d["C"], self.sig_ag, self.sig_ag.next_epoch(), None,
-                         stream)
+    def opts(self, **kw):
+        """The layer's options (its skew schedule, if any, plus kw), built once."""
+        key = tuple(sorted(kw.items()))
+        if key not in self._opts:
+            self._opts[key] = skew_opts(self.api, self.cfg, **kw)
+        return self._opts[key]
 
-    def rs(self, stream=None, b=0):
-        r = self.rs_d
-        self.api.gemm_rs(self.bufs[b]["rs_heap"], r["rank_off"], r["a_off"], r["b_off"],
-                         r["out_off"], r["M"], r["N"], r["K_r"], self.sig_rs,
-                         self.sig_rs.next_epoch(), None, stream)
+    def launch(self, stream=None, b=0, epoch=None, **kw):
+        d, x = self.d, self.bufs[b]
+        e = self.sig.next_epoch() if epoch is None else epoch
+        self.api.ag_gemm(x["heap"], d["rank_off"], d["a_off"], d["M_r"], d["N"], d["K"], x["B"],
+                         x["G"], x["C"], self.sig, e, self.opts(**kw), stream)
 
     def check(self):
-        for s in (self.sig_ag, self.sig_rs):
-            st = s.status()
-            if st[0] != self.api.OK:
-                raise RuntimeError(f"device error latched during the benchmark: {st}")
+        st = self.sig.status()
+        if st[0] != self.api.OK:
+            raise RuntimeError(f"{self.name}: device error latched during the benchmark: {st}")
+
+    def close(self):
+        self.sig.close()
+        self.bufs = []
+
+
+class TpLayer:
+    """The tp_layer step on the device: AG-GEMM TP then GEMM-RS TP, each with
+    its own signal object."""
+
+    def __init__(self, api, torch, seed=0):
+        from overlap_producer_warps_gb300 import inputs
+        self.api, self.torch = api, torch
+        self.ag = AgLayer(api, torch, "ag_tp", seed=seed)
+        self.rs_cfg = inputs.CONFIGS["rs_tp"]
+        self.rs_d = inputs.rs_inputs(self.rs_cfg, seed=seed)
+        self.rs_heap = torch.from_numpy(self.rs_d["heap"]).cuda()
+        r = self.rs_d
+        self.sig_rs = api.Signal(api.rs_num_flags(r["R"], r["M"], r["N"]))
+        self.flops = self.ag.flops + flops_rs(self.rs_cfg)
+
+    def rs(self, stream=None):
+        r = self.rs_d
+        self.api.gemm_rs(self.rs_heap, r["rank_off"], r["a_off"], r["b_off"], r["out_off"], r["M"],
+                         r["N"], r["K_r"], self.sig_rs, self.sig_rs.next_epoch(), None, stream)
+
+    def step(self):
+        self.ag.launch()
+        self.rs()
+
+    def check(self):
+        self.ag.check()
+        st = self.sig_rs.status()
+        if st[0] != self.api.OK:
+            raise RuntimeError(f"rs_tp: device error latched during the benchmark: {st}")
+
+    def close(self):
+        self.ag.close()
+        self.sig_rs.close()
 
 
 def time_launches(torch, fn, n, warm=2):
-    """Mean device time (ms) per launch over n back-to-back launches of fn(),
-    timed with events on the current stream.  A short spin kernel ahead of
-    the first event keeps the GPU busy while the host enqueues the launches,
-    so neither the first launch's host-side cost nor its launch latency
-    falls inside the interval."""
+    """Device time (ms) of each of n back-to-back calls of fn(), from CUDA
+    events recorded between them on the current stream: mean, median and
+    min.  A short spin kernel ahead of the first event keeps the GPU busy
+    while the host enqueues the calls, so neither the first call's host-side
+    cost nor its launch latency falls inside an interval."""
     s = torch.cuda.current_stream()
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    # about 0.3 ms + 0.1 ms per launch at 2 GHz: more than the host needs
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    # about 0.3 ms + 0.1 ms per call at 2 GHz: more than the host needs
     spin = getattr(torch.cuda, "_sleep", None)
     if spin is not None:
         spin(int(2e9 * (3e-4 + 1e-4 * n)))
-    e0.record(s)
-    for _ in range(n):
+    ev[0].record(s)
+    for i in range(n):
         fn()
-    e1.record(s)
-    e1.synchronize()
-    return e0.elapsed_time(e1) / n
+        ev[i + 1].record(s)
+    ev[n].synchronize()
+    t = [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+    return {"mean": statistics.mean(t), "median": statistics.median(t), "min": min(t), "n": n}
+
+
+def tflops_of(flops, t):
+    """TFLOP/s at the median (and best) time of a time_launches() result."""
+    return {"tflops": flops / t["median"] / 1e9, "tflops_best": flops / t["min"] / 1e9}
 
 
 def ring_results(api, torch, reps, R=8, n=8 * (1 << 21)):
@@ -341,8 +404,8 @@ def ring_results(api, torch, reps, R=8, n=8 * (1 << 21)):
     # per rank: send own chunk (r+w), R-2 forwarding reduce steps (2r+w), the last
     # reduce step (2r+2w), R-2 forwarding gather steps (r+2w), the last gather step (r+w)
     algo_bytes = R * chunk_b * (2 + 3 * (R - 2) + 4 + 3 * (R - 2) + 2)
-    gbs = algo_bytes / (t * 1e-3) / 1e9
-    busbw = 2 * (R - 1) / R * n * 4 / (t * 1e-3) / 1e9
+    gbs = algo_bytes / (t["median"] * 1e-3) / 1e9
+    busbw = 2 * (R - 1) / R * n * 4 / (t["median"] * 1e-3) / 1e9
     sig.close()
     return {"ranks": R, "values_per_rank": n, "ms": t, "hbm_gbs": gbs,
             "hbm_frac": gbs / float(peaks["hbm_gbs"]), "algo_bytes": algo_bytes,
@@ -365,7 +428,7 @@ def alltoall_results(api, torch, reps, R=8, B=8 << 20):
     if st[0] != api.OK:
         raise RuntimeError(f"alltoall: device error {st}")
     moved = 2 * R * R * B  # every slice read once and written once
-    gbs = moved / (t * 1e-3) / 1e9
+    gbs = moved / (t["median"] * 1e-3) / 1e9
     sig.close()
     return {"ranks": R, "bytes_per_slice": B, "ms": t, "hbm_gbs": gbs,
             "hbm_frac": gbs / float(peaks["hbm_gbs"])}
@@ -374,31 +437,15 @@ def alltoall_results(api, torch, reps, R=8, B=8 << 20):
 def ag_fused_results(api, torch, name, reps, producer_only=False):
     """Fused AG-GEMM launches of one layer alone (its skew schedule included),
     or, with producer_only, its gather leg alone (GB/s of shard read + G write)."""
-    from overlap_producer_warps_gb300 import inputs
-    cfg = inputs.CONFIGS[name]
-    d = inputs.ag_inputs(cfg, seed=0)
-    R, M_r, K, N = cfg["R"], cfg["M_r"], cfg["K"], cfg["N"]
-    dev = torch.device("cuda")
-    heap = torch.from_numpy(d["heap"]).to(dev)
-    B = torch.from_numpy(d["B"].view(np.int16)).to(dev).view(torch.bfloat16)
-    G = torch.empty((R * M_r, K), dtype=torch.bfloat16, device=dev)
-    C = torch.empty((R * M_r, N), dtype=torch.bfloat16, device=dev)
-    sig = api.Signal(api.ag_num_flags(R, M_r, K))
-    kw = {}
-    if cfg.get("skew"):
-        perm, delay = inputs.skew_schedule(0, R)
-        kw = dict(publish_perm=perm, delay_ns=delay)
+    w = AgLayer(api, torch, name)
+    kw = {"role": api.ROLE_PRODUCER} if producer_only else {}
+    t = time_launches(torch, lambda: w.launch(**kw), reps)
+    w.check()
+    d = w.d
+    w.close()
     if producer_only:
-        kw["role"] = api.ROLE_PRODUCER
-    t = time_launches(torch, lambda: api.ag_gemm(heap, d["rank_off"], d["a_off"], M_r, N, K, B, G, C,
-                                                 sig, sig.next_epoch(), api.make_opts(**kw)), reps)
-    st = sig.status()
-    if st[0] != api.OK:
-        raise RuntimeError(f"{name}: device error {st}")
-    sig.close()
-    if producer_only:
-        return {"ms": t, "gather_hbm_gbs": 2.0 * R * M_r * K * 2 / (t * 1e-3) / 1e9}
-    return {"ms": t, "tflops": flops_ag(cfg) / t / 1e9}
+        return {"ms": t, "gather_hbm_gbs": 2.0 * w.M * d["K"] * 2 / (t["median"] * 1e-3) / 1e9}
+    return {"ms": t, **tflops_of(w.flops, t)}
 
 
 def rs_results(api, torch, reps, scatter_only=False):
@@ -419,141 +466,123 @@ def rs_results(api, torch, reps, scatter_only=False):
         raise RuntimeError(f"rs_tp: device error {st}")
     sig.close()
     if scatter_only:
-        return {"ms": t, "scatter_hbm_gbs": M * N * 2 / (t * 1e-3) / 1e9}
-    return {"ms": t, "tflops": flops_rs(cfg) / t / 1e9}
+        return {"ms": t, "scatter_hbm_gbs": M * N * 2 / (t["median"] * 1e-3) / 1e9}
+    return {"ms": t, **tflops_of(flops_rs(cfg), t)}
 
 
 def tiny_results(api, torch, reps=50):
     """The tiny AG-GEMM configuration (R=2, 64x128 shards, K=N=128), which is
     bound by latency: the device time per launch back to back, and the time
     from the host call to the completed launch (call, then synchronise)."""
-    import time as _time
-    from overlap_producer_warps_gb300 import inputs
-    cfg = inputs.CONFIGS["ag_tiny"]
-    d = inputs.ag_inputs(cfg, seed=0)
-    R, M_r, K, N = cfg["R"], cfg["M_r"], cfg["K"], cfg["N"]
-    heap = torch.from_numpy(d["heap"]).cuda()
-    B = torch.from_numpy(d["B"].view(np.int16)).cuda().view(torch.bfloat16)
-    G = torch.empty((R * M_r, K), dtype=torch.bfloat16, device="cuda")
-    C = torch.empty((R * M_r, N), dtype=torch.bfloat16, device="cuda")
-    sig = api.Signal(api.ag_num_flags(R, M_r, K))
-
-    def run():
-        api.ag_gemm(heap, d["rank_off"], d["a_off"], M_r, N, K, B, G, C, sig, sig.next_epoch())
-
-    t_dev = time_launches(torch, run, reps)
+    w = AgLayer(api, torch, "ag_tiny")
+    t_dev = time_launches(torch, w.launch, reps)
     for _ in range(3):
-        run()
+        w.launch()
     torch.cuda.synchronize()
     lat = []
     for _ in range(reps):
-        t0 = _time.perf_counter()
-        run()
+        t0 = time.perf_counter()
+        w.launch()
         torch.cuda.synchronize()
-        lat.append(_time.perf_counter() - t0)
-    st = sig.status()
-    if st[0] != api.OK:
-        raise RuntimeError(f"ag_tiny: device error {st}")
-    sig.close()
+        lat.append(time.perf_counter() - t0)
+    w.check()
+    w.close()
     lat.sort()
-    return {"us_per_launch_back_to_back": t_dev * 1e3,
+    return {"us_per_launch_back_to_back_median": t_dev["median"] * 1e3,
+            "us_per_launch_back_to_back_min": t_dev["min"] * 1e3,
             "us_call_to_done_median": lat[len(lat) // 2] * 1e6,
             "us_call_to_done_min": lat[0] * 1e6}
 
 
-def per_config_results(api, torch, peak_tflops, reps=5):
-    """Each of the pages' tensor-parallel configurations on its own: fused
-    TFLOP/s, the unfused copy-then-GEMM baseline, cuBLAS on the pre-gathered
-    matrix, and the AG overlap efficiency."""
+def mm_f32_out(torch):
+    """A bf16 x bf16 -> fp32 product on the GPU, as cuBLAS gives it: torch.mm
+    with out_dtype where this PyTorch has it, else the bf16 product widened
+    (lower precision; named in the result)."""
+    a = torch.zeros((16, 16), dtype=torch.bfloat16, device="cuda")
+    try:
+        torch.mm(a, a, out_dtype=torch.float32)
+        return (lambda x, y: torch.mm(x, y, out_dtype=torch.float32)), "torch.mm(out_dtype=float32)"
+    except (TypeError, RuntimeError):
+        return (lambda x, y: torch.matmul(x, y).float()), "bf16 matmul widened to fp32"
+
+
+def ag_config_results(api, torch, name, peak_tflops, reps):
+    """One AG-GEMM layer: fused (default schedule), the page's static swizzle,
+    serial sync, batched row signals, the legs alone, unfused copy-then-GEMM
+    and cuBLAS on the pre-gathered G, each over `reps` launches."""
+    w = AgLayer(api, torch, name)
+    d, cfg = w.d, w.cfg
+    R, M_r, K, N = d["R"], d["M_r"], d["K"], d["N"]
+    x = w.bufs[0]
+    t = {}
+    t["fused"] = time_launches(torch, w.launch, reps)
+    t["swizzle"] = time_launches(torch, lambda: w.launch(schedule=api.SCHED_SWIZZLE), reps)
+    # every consumer waits for the whole gather before its first tile
+    t["serial"] = time_launches(torch, lambda: w.launch(sync_mode=api.SYNC_SERIAL), reps)
+    sig_add = api.Signal(api.ag_num_row_counters(R, M_r, K))
+
+    def fused_row_add():
+        api.ag_gemm(x["heap"], d["rank_off"], d["a_off"], M_r, N, K, x["B"], x["G"], x["C"],
+                    sig_add, sig_add.next_epoch(),
+                    skew_opts(api, cfg, signal_mode=api.SIGNAL_ROW_ADD))
+
+    t["row_add"] = time_launches(torch, fused_row_add, reps)
+    if sig_add.status()[0] != api.OK:
+        raise RuntimeError(f"{name}: device error with row-ADD signals")
+    sig_add.close()
+    if cfg.get("skew"):
+        # the publish order without the per-rank delays
+        from overlap_producer_warps_gb300 import inputs
+        perm, _ = inputs.skew_schedule(0, R)
+        t["no_delay"] = time_launches(torch, lambda: api.ag_gemm(
+            x["heap"], d["rank_off"], d["a_off"], M_r, N, K, x["B"], x["G"], x["C"], w.sig,
+            w.sig.next_epoch(), api.make_opts(publish_perm=perm)), reps)
+    t["producer_only"] = time_launches(torch, lambda: w.launch(role=api.ROLE_PRODUCER), reps)
+    t["consumer_only"] = time_launches(
+        torch, lambda: w.launch(epoch=w.sig.next_epoch() - 1, role=api.ROLE_CONSUMER), reps)
+    w.check()
+    shards = [x["heap"][int(d["rank_off"][r]):int(d["rank_off"][r]) + M_r * K * 2]
+              .view(torch.bfloat16).view(M_r, K) for r in range(R)]
+    G, B, C = x["G"], x["B"], x["C"]
+
+    def unfused():
+        for r in range(R):
+            G[r * M_r:(r + 1) * M_r].copy_(shards[r])
+        torch.matmul(G, B, out=C)
+
+    t["unfused"] = time_launches(torch, unfused, reps)
+    t["gemm_only"] = time_launches(torch, lambda: torch.matmul(G, B, out=C), reps)
+    fl = w.flops
+    med = {k: v["median"] for k, v in t.items()}
+    e = (med["producer_only"] + med["consumer_only"] - med["fused"]) / min(
+        med["producer_only"], med["consumer_only"])
+    out = {
+        "fused_tflops": fl / med["fused"] / 1e9,
+        "fused_tflops_best": fl / t["fused"]["min"] / 1e9,
+        "pct_of_peak": fl / med["fused"] / 1e9 / peak_tflops,
+        "swizzle_schedule_tflops": fl / med["swizzle"] / 1e9,
+        "serial_sync_tflops": fl / med["serial"] / 1e9,
+        "row_add_signal_tflops": fl / med["row_add"] / 1e9,
+        "unfused_copy_then_gemm_tflops": fl / med["unfused"] / 1e9,
+        "cublas_gemm_only_tflops": fl / med["gemm_only"] / 1e9,
+        "fused_vs_cublas_gemm_only": med["gemm_only"] / med["fused"],
+        "ms": t,
+        "overlap_efficiency": max(0.0, min(1.0, e)),
+        "gather_hbm_gbs_producer_only": 2.0 * w.M * K * 2 / (med["producer_only"] * 1e-3) / 1e9,
+    }
+    if "no_delay" in med:
+        out["no_delay_fused_tflops"] = fl / med["no_delay"] / 1e9
+    del shards, G, B, C, x
+    w.close()
+    torch.cuda.empty_cache()
+    return out
+
+
+def rs_config_results(api, torch, peak_tflops, reps):
+    """GEMM-RS TP: fused, the legs alone, the unfused path (fp32 partials, an
+    fp32 sum in rank order, then the row blocks split off) and one cuBLAS GEMM
+    with the same FLOPs."""
     from overlap_producer_warps_gb300 import inputs
-    out = {}
-    for name in ("ag_tp", "ag_mlp", "ag_skew"):
-        cfg = inputs.CONFIGS[name]
-        d = inputs.ag_inputs(cfg, seed=0)
-        R, M_r, K, N = cfg["R"], cfg["M_r"], cfg["K"], cfg["N"]
-        M = R * M_r
-        heap = torch.from_numpy(d["heap"]).cuda()
-        B = torch.from_numpy(d["B"].view(np.int16)).cuda().view(torch.bfloat16)
-        G = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
-        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        sig = api.Signal(api.ag_num_flags(R, M_r, K))
-        skew = {}
-        if cfg.get("skew"):
-            perm, delay = inputs.skew_schedule(0, R)
-            skew = dict(publish_perm=perm, delay_ns=delay)
-
-        def fused(**kw):
-            o = api.make_opts(**skew, **kw)
-            api.ag_gemm(heap, d["rank_off"], d["a_off"], M_r, N, K, B, G, C, sig,
-                        sig.next_epoch(), o)
-
-        def producer_only():
-            api.ag_gemm(heap, d["rank_off"], d["a_off"], M_r, N, K, B, G, C, sig,
-                        sig.next_epoch(), api.make_opts(role=api.ROLE_PRODUCER, **skew))
-
-        def consumer_only():
-            api.ag_gemm(heap, d["rank_off"], d["a_off"], M_r, N, K, B, G, C, sig,
-                        sig.next_epoch() - 1, api.make_opts(role=api.ROLE_CONSUMER, **skew))
-
-        t_fused = time_launches(torch, fused, reps)
-        t_swz = time_launches(torch, lambda: fused(schedule=api.SCHED_SWIZZLE), reps)
-        # every consumer waits for the whole gather before its first tile
-        t_serial = time_launches(torch, lambda: fused(sync_mode=api.SYNC_SERIAL), reps)
-        sig_add = api.Signal(api.ag_num_row_counters(R, M_r, K))
-
-        def fused_row_add():
-            api.ag_gemm(heap, d["rank_off"], d["a_off"], M_r, N, K, B, G, C, sig_add,
-                        sig_add.next_epoch(), api.make_opts(signal_mode=api.SIGNAL_ROW_ADD, **skew))
-
-        t_add = time_launches(torch, fused_row_add, reps)
-        # the skew layer with its publish order but without the per-rank delays
-        t_nodelay = (time_launches(torch, lambda: api.ag_gemm(
-            heap, d["rank_off"], d["a_off"], M_r, N, K, B, G, C, sig, sig.next_epoch(),
-            api.make_opts(publish_perm=skew["publish_perm"])), reps) if skew else None)
-        if sig_add.status()[0] != api.OK:
-            raise RuntimeError(f"{name}: device error with row-ADD signals")
-        sig_add.close()
-        t_prod = time_launches(torch, producer_only, reps)
-        t_cons = time_launches(torch, consumer_only, reps)
-        st = sig.status()
-        if st[0] != api.OK:
-            raise RuntimeError(f"{name}: device error {st}")
-        shards = [heap[int(d["rank_off"][r]):int(d["rank_off"][r]) + M_r * K * 2]
-                  .view(torch.bfloat16).view(M_r, K) for r in range(R)]
-
-        def unfused():
-            for r in range(R):
-                G[r * M_r:(r + 1) * M_r].copy_(shards[r])
-            torch.matmul(G, B, out=C)
-
-        t_unf = time_launches(torch, unfused, reps)
-        t_gemm = time_launches(torch, lambda: torch.matmul(G, B, out=C), reps)
-        fl = flops_ag(cfg)
-        e = (t_prod + t_cons - t_fused) / min(t_prod, t_cons)
-        out[name] = {
-            "fused_tflops": fl / t_fused / 1e9, "pct_of_peak": fl / t_fused / 1e9 / peak_tflops,
-            "swizzle_schedule_tflops": fl / t_swz / 1e9,
-            "serial_sync_tflops": fl / t_serial / 1e9,
-            "row_add_signal_tflops": fl / t_add / 1e9,
-            "unfused_copy_then_gemm_tflops": fl / t_unf / 1e9,
-            "cublas_gemm_only_tflops": fl / t_gemm / 1e9,
-            "ms": {"fused": t_fused, "swizzle": t_swz, "serial": t_serial, "row_add": t_add,
-                   "producer_only": t_prod,
-                   "consumer_only": t_cons, "unfused": t_unf, "gemm_only": t_gemm},
-            "overlap_efficiency": max(0.0, min(1.0, e)),
-            "gather_hbm_gbs_producer_only": 2.0 * M * K * 2 / (t_prod * 1e-3) / 1e9,
-        }
-        if t_nodelay is not None:
-            out[name]["no_delay_fused_tflops"] = fl / t_nodelay / 1e9
-            out[name]["ms"]["no_delay"] = t_nodelay
-        sig.close()
-        del heap, B, G, C, shards
-        torch.cuda.empty_cache()
-
-    out["ag_tiny"] = tiny_results(api, torch)
-    out["ring_allreduce"] = ring_results(api, torch, reps)
-    out["alltoall"] = alltoall_results(api, torch, reps)
-
     cfg = inputs.CONFIGS["rs_tp"]
     d = inputs.rs_inputs(cfg, seed=0)
     R, M, K_r, N = cfg["R"], cfg["M"], cfg["K_r"], cfg["N"]
@@ -564,73 +593,94 @@ def per_config_results(api, torch, peak_tflops, reps=5):
         api.gemm_rs(heap, d["rank_off"], d["a_off"], d["b_off"], d["out_off"], M, N, K_r, sig,
                     sig.next_epoch(), api.make_opts(role=role))
 
-    t_fused = time_launches(torch, rs, reps)
-    t_gemm_leg = time_launches(torch, lambda: rs(api.ROLE_PRODUCER), reps)
-    t_scatter_leg = time_launches(torch, lambda: rs(api.ROLE_CONSUMER), reps)
+    t = {}
+    t["fused"] = time_launches(torch, rs, reps)
+    t["gemm_leg_only"] = time_launches(torch, lambda: rs(api.ROLE_PRODUCER), reps)
+    t["scatter_leg_only"] = time_launches(torch, lambda: rs(api.ROLE_CONSUMER), reps)
     A = [heap[int(d["rank_off"][r]) + d["a_off"]:int(d["rank_off"][r]) + d["a_off"] + M * K_r * 2]
          .view(torch.bfloat16).view(M, K_r) for r in range(R)]
     Bs = [heap[int(d["rank_off"][r]) + d["b_off"]:int(d["rank_off"][r]) + d["b_off"] + K_r * N * 2]
           .view(torch.bfloat16).view(K_r, N) for r in range(R)]
     outs = [heap[int(d["rank_off"][j]) + d["out_off"]:int(d["rank_off"][j]) + d["out_off"]
                  + (M // R) * N * 2].view(torch.bfloat16).view(M // R, N) for j in range(R)]
+    mm32, mm32_name = mm_f32_out(torch)
 
     def unfused_rs():
-        S = torch.matmul(A[0], Bs[0]).float()
+        S = mm32(A[0], Bs[0])
         for r in range(1, R):
-            S += torch.matmul(A[r], Bs[r]).float()
+            S += mm32(A[r], Bs[r])
         for j in range(R):
             outs[j].copy_(S[j * (M // R):(j + 1) * (M // R)])
 
-    t_unf = time_launches(torch, unfused_rs, reps)
+    t["unfused"] = time_launches(torch, unfused_rs, reps)
     # The same FLOPs as one cuBLAS GEMM with the ranks' K slices side by side
     # ([M, R*K_r] @ [R*K_r, N]): no per-rank partials, no reduction, no scatter.
     A_cat = torch.cat(A, dim=1)
     B_cat = torch.cat(Bs, dim=0)
     C_cat = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    t_gemm = time_launches(torch, lambda: torch.matmul(A_cat, B_cat, out=C_cat), reps)
+    t["gemm_only"] = time_launches(torch, lambda: torch.matmul(A_cat, B_cat, out=C_cat), reps)
     del A_cat, B_cat, C_cat
     st = sig.status()
     if st[0] != api.OK:
         raise RuntimeError(f"rs_tp: device error {st}")
     fl = flops_rs(cfg)
-    e = (t_gemm_leg + t_scatter_leg - t_fused) / min(t_gemm_leg, t_scatter_leg)
-    out["rs_tp"] = {"fused_tflops": fl / t_fused / 1e9, "pct_of_peak": fl / t_fused / 1e9 / peak_tflops,
-                    "unfused_partials_then_sum_tflops": fl / t_unf / 1e9,
-                    "cublas_single_gemm_tflops": fl / t_gemm / 1e9,
-                    "ms": {"fused": t_fused, "gemm_leg_only": t_gemm_leg,
-                           "scatter_leg_only": t_scatter_leg, "unfused": t_unf,
-                           "gemm_only": t_gemm},
-                    "overlap_efficiency": max(0.0, min(1.0, e)),
-                    "scatter_hbm_gbs_scatter_only": M * N * 2 / (t_scatter_leg * 1e-3) / 1e9}
+    med = {k: v["median"] for k, v in t.items()}
+    e = (med["gemm_leg_only"] + med["scatter_leg_only"] - med["fused"]) / min(
+        med["gemm_leg_only"], med["scatter_leg_only"])
     sig.close()
+    return {"fused_tflops": fl / med["fused"] / 1e9,
+            "fused_tflops_best": fl / t["fused"]["min"] / 1e9,
+            "pct_of_peak": fl / med["fused"] / 1e9 / peak_tflops,
+            "unfused_partials_then_sum_tflops": fl / med["unfused"] / 1e9,
+            "unfused_partials": mm32_name,
+            "cublas_single_gemm_tflops": fl / med["gemm_only"] / 1e9,
+            "ms": t,
+            "overlap_efficiency": max(0.0, min(1.0, e)),
+            "scatter_hbm_gbs_scatter_only": M * N * 2 / (med["scatter_leg_only"] * 1e-3) / 1e9}
+
+
+def tp_layer_results(api, torch, peak_tflops, reps):
+    """The tp_layer step (AG-GEMM TP then GEMM-RS TP) back to back."""
+    w = TpLayer(api, torch)
+    t = time_launches(torch, w.step, reps)
+    w.check()
+    fl = w.flops
+    w.close()
+    return {"workload": TP_WORKLOAD, "step_tflops": fl / t["median"] / 1e9,
+            "step_tflops_best": fl / t["min"] / 1e9,
+            "pct_of_peak": fl / t["median"] / 1e9 / peak_tflops, "ms": t}
+
+
+def per_config_results(api, torch, peak_tflops, reps=20):
+    """Each of the pages' tensor-parallel configurations on its own, burst
+    (short runs against the burst peak): fused TFLOP/s at the median launch,
+    the unfused baselines, cuBLAS with the same FLOPs, overlap efficiency."""
+    out = {}
+    for name in ("ag_tp", "ag_mlp", "ag_skew"):
+        out[name] = ag_config_results(api, torch, name, peak_tflops, reps)
+    out["rs_tp"] = rs_config_results(api, torch, peak_tflops, reps)
+    out["tp_layer"] = tp_layer_results(api, torch, peak_tflops, reps)
+    out["ag_tiny"] = tiny_results(api, torch)
+    out["ring_allreduce"] = ring_results(api, torch, reps)
+    out["alltoall"] = alltoall_results(api, torch, reps)
     return out
 
 
-def e2e_results(torch, w, args, dist, world, flops_step):
-    """The step through the public API with its inputs and results in pinned
-    host memory.  Every step copies its inputs host -> device, runs AG-GEMM
-    and GEMM-RS, and reads C and every rank's output block back.  The steps
-    are pipelined over two device buffer sets and three streams: step i+1's
-    inputs go in and step i-1's results come out while step i computes.
-    The timed region runs from before step 0's first input copy to after the
-    last step's last result copy."""
-    a, r = w.ag_d, w.rs_d
-    h_ag = torch.from_numpy(a["heap"]).pin_memory()
-    h_B = torch.from_numpy(a["B"].view(np.int16)).pin_memory()
-    h_rs = torch.from_numpy(r["heap"]).pin_memory()
-    rs_in = []  # (offset, nbytes) of every A_r and B_r region
-    for rr in range(r["R"]):
-        o = int(r["rank_off"][rr])
-        rs_in.append((o + r["a_off"], r["M"] * r["K_r"] * 2))
-        rs_in.append((o + r["b_off"], r["K_r"] * r["N"] * 2))
-    Mb = r["M"] // r["R"]
+def e2e_results(torch, w, args, dist, world):
+    """The headline step through the public API with its inputs and result in
+    pinned host memory.  Every step copies the shards and B host -> device,
+    runs AG-GEMM and reads C back.  The steps are pipelined over two device
+    buffer sets and three streams: step i+1's inputs go in and step i-1's
+    result comes out while step i computes.  The timed region runs from
+    before step 0's first input copy to after the last step's result copy."""
+    d = w.d
+    h_heap = torch.from_numpy(d["heap"]).pin_memory()
+    h_B = torch.from_numpy(d["B"].view(np.int16)).pin_memory()
     nsets = len(w.bufs)
     h_C = [torch.empty(w.bufs[0]["C"].shape, dtype=torch.bfloat16).pin_memory()
            for _ in range(nsets)]
-    h_out = [torch.empty((r["R"], Mb * r["N"] * 2), dtype=torch.uint8).pin_memory()
-             for _ in range(nsets)]
-    h2d = h_ag.numel() + h_B.numel() * 2 + sum(n for _, n in rs_in)
-    d2h = h_C[0].numel() * 2 + h_out[0].numel()
+    h2d = h_heap.numel() + h_B.numel() * 2
+    d2h = h_C[0].numel() * 2
     stream, s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event(enable_timing=False)
     in_done = [ev() for _ in range(nsets)]
@@ -640,28 +690,22 @@ def e2e_results(torch, w, args, dist, world, flops_step):
 
     def e2e_step(i):
         b = i % nsets
-        d = w.bufs[b]
+        x = w.bufs[b]
         with torch.cuda.stream(s_in):
             if used[b]:
                 s_in.wait_event(comp_done[b])  # step i-2 has finished reading set b
-            d["ag_heap"].copy_(h_ag, non_blocking=True)
-            d["B"].view(torch.int16).copy_(h_B, non_blocking=True)
-            for o, n in rs_in:
-                d["rs_heap"][o:o + n].copy_(h_rs[o:o + n], non_blocking=True)
+            x["heap"].copy_(h_heap, non_blocking=True)
+            x["B"].view(torch.int16).copy_(h_B, non_blocking=True)
             in_done[b].record(s_in)
         stream.wait_event(in_done[b])
         if used[b]:
-            stream.wait_event(out_done[b])  # step i-2's results are on the host
-        w.ag(stream, b)
-        w.rs(stream, b)
+            stream.wait_event(out_done[b])  # step i-2's result is on the host
+        w.launch(stream, b)
         comp_done[b].record(stream)
         used[b] = True
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[b])
-            h_C[b].copy_(d["C"], non_blocking=True)
-            for j in range(r["R"]):
-                o = int(r["rank_off"][j]) + r["out_off"]
-                h_out[b][j].copy_(d["rs_heap"][o:o + Mb * r["N"] * 2], non_blocking=True)
+            h_C[b].copy_(x["C"], non_blocking=True)
             out_done[b].record(s_out)
 
     def run(n, e0=None, e1=None):
@@ -686,9 +730,10 @@ def e2e_results(torch, w, args, dist, world, flops_step):
     torch.cuda.synchronize()
     w.check()
     t_e2e = reduce_max(e0.elapsed_time(e1) / args.steps, dist, "cuda")
-    return {"value": whole_job_tflops(world, flops_step, t_e2e), "unit": UNIT,
+    return {"value": whole_job_tflops(world, w.flops, t_e2e), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "ms_per_step": t_e2e, "pipelined": f"{nsets} buffer sets, copy-in / compute / copy-out streams"}
+            "ms_per_step": t_e2e,
+            "pipelined": f"{nsets} buffer sets, copy-in / compute / copy-out streams"}
 
 
 def run_ours(args, rank, world, dist):
@@ -709,87 +754,89 @@ def run_ours(args, rank, world, dist):
     step_peak_name = ("bf16_tflops_sustained (cuBLAS back to back, under the power cap)"
                       if sustained else "bf16_tflops (burst, cuBLAS)")
 
-    w = TpLayer(api, torch, sets=2)
+    w = AgLayer(api, torch, HEADLINE, sets=2)
     stream = torch.cuda.current_stream()
-
-    def step(evs=None):
-        if evs is not None:
-            evs[0].record(stream)
-        w.ag()
-        if evs is not None:
-            evs[1].record(stream)
-        w.rs()
-        if evs is not None:
-            evs[2].record(stream)
-
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
+    t_load0 = time.monotonic()
     # An idle GPU needs seconds of load before its clocks settle: run the
     # step, untimed, for args.prewarm_s before the W counted warm-up steps.
     t_pre = time.perf_counter() + args.prewarm_s
     while time.perf_counter() < t_pre:
-        for _ in range(10):
-            step()
+        for _ in range(4):
+            w.launch()
         torch.cuda.synchronize()
     for _ in range(args.warmup):
-        step()
+        w.launch()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    start.record(stream)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    t_timed0 = time.monotonic()
+    ev[0].record(stream)
     for i in range(args.steps):
-        step(evs[i])
-    end.record(stream)
+        w.launch()
+        ev[i + 1].record(stream)
     torch.cuda.synchronize()
+    t_timed1 = time.monotonic()
     if dist is not None:
         dist.barrier()
-    clocks = sampler.stop()
     w.check()
-    ms_total = start.elapsed_time(end)
-    ag_all = [e[0].elapsed_time(e[1]) for e in evs]
-    rs_all = [e[1].elapsed_time(e[2]) for e in evs]
-    ag_ms, rs_ms = statistics.mean(ag_all), statistics.mean(rs_all)
+    launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    ms_total = ev[0].elapsed_time(ev[args.steps])
     t_step = reduce_max(ms_total / args.steps, dist, "cuda")
-    flops_step = w.flops_ag + w.flops_rs
-    value = whole_job_tflops(world, flops_step, t_step)
+    value = whole_job_tflops(world, w.flops, t_step)
 
     # ---- end to end through the public API with host buffers
-    e2e = e2e_results(torch, w, args, dist, world, flops_step)
+    e2e = e2e_results(torch, w, args, dist, world)
+    sampler.stop()
+    # the timed window's own samples; the load samples since the pre-warm began
+    clocks = sampler.summary(t_timed0, t_timed1)
+    clocks["under_load_since_prewarm"] = sampler.summary(t_load0, t_timed1)
 
-    # ---- roofline of the dominant kernel (device time share)
-    dom = "gemm_rs" if rs_ms >= ag_ms else "ag_gemm"
-    dom_ms = rs_ms if dom == "gemm_rs" else ag_ms
-    dom_flops = w.flops_rs if dom == "gemm_rs" else w.flops_ag
-    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": step_peak,
+    # ---- roofline of the step's one kernel
+    mean_ms = statistics.mean(launch_ms)
+    achieved = w.flops / (mean_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "ag_gemm", "achieved": achieved, "peak": step_peak,
                 "unit": "TFLOP/s", "frac": achieved / step_peak,
                 "peak_source": f"{peak_src} {step_peak_name}",
-                "traffic": kernel_traffic(dom),
-                "ms_per_launch": {"ag_gemm": ag_ms, "gemm_rs": rs_ms},
-                "ms_per_launch_median": {"ag_gemm": statistics.median(ag_all),
-                                         "gemm_rs": statistics.median(rs_all)},
-                "ms_per_launch_min": {"ag_gemm": min(ag_all), "gemm_rs": min(rs_all)}}
+                "traffic": kernel_traffic("ag_gemm"),
+                "ms_per_launch": mean_ms, "ms_per_launch_median": statistics.median(launch_ms),
+                "ms_per_launch_min": min(launch_ms)}
 
+    d = w.d
+    perm, delay = None, None
+    from overlap_producer_warps_gb300 import inputs
+    if w.cfg.get("skew"):
+        perm, delay = inputs.skew_schedule(0, d["R"])
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "impl": "ours",
-            "config": {"workload": WORKLOAD, "R": 8, "epochs": "fresh epoch per launch, no reset",
-                       "l2": "inputs larger than L2 (656 MiB read per step vs 129 MB L2)",
+            "config": {"workload": WORKLOAD, "R": d["R"], "M_r": d["M_r"], "K": d["K"],
+                       "N": d["N"], "schedule": "ready (default)",
+                       "publish_perm": None if perm is None else [int(v) for v in perm],
+                       "delay_us": None if delay is None else [int(v) // 1000 for v in delay],
+                       "epochs": "fresh epoch per launch, no reset",
+                       "l2": "inputs larger than L2 (1.74 GB of algorithmic traffic per step "
+                             "vs 129 MB L2)",
                        "prewarm_s": args.prewarm_s,
                        "parallelism": f"replicas x{world}"},
             "pct_of_peak": value / world / step_peak,
-            "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks}
+            "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks}
+    w.close()
+    del w
+    torch.cuda.empty_cache()
 
     if rank == 0 and world == 1 and not args.no_extra:
+        sampler2 = ClockSampler(torch.cuda.current_device())
+        sampler2.start()
         line["per_config"] = per_config_results(api, torch, peak)
+        sampler2.stop()
+        line["per_config"]["clocks"] = sampler2.summary()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_sample(w.ag_d, w.rs_d, w.ag_cfg, w.rs_cfg,
-                                             min_seconds=args.cpu_seconds)
+        line["cpu_baseline"] = oracle_sample(d, min_seconds=args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -806,9 +853,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--prewarm-s", type=float, default=2.0,
                     help="seconds of untimed steps before the warm-up steps (clock ramp)")
-    ap.add_argument("--only", choices=["ring_allreduce", "alltoall", "ag_tiny", "ag_tp", "ag_mlp", "ag_skew",
-                                       "ag_tp_gather", "ag_mlp_gather", "ag_skew_gather",
-                                       "rs_tp", "rs_tp_scatter"],
+    ap.add_argument("--only", choices=["ring_allreduce", "alltoall", "ag_tiny", "ag_tp", "ag_mlp",
+                                       "ag_skew", "ag_tp_gather", "ag_mlp_gather",
+                                       "ag_skew_gather", "rs_tp", "rs_tp_scatter", "tp_layer",
+                                       "ag_tp_all", "ag_mlp_all", "ag_skew_all", "rs_tp_all"],
                     default=None,
                     help="run only this per-configuration measurement (for profiling) and "
                          "print its result as one JSON line")
@@ -824,20 +872,29 @@ def main():
     if args.only is not None:
         import torch
         from overlap_producer_warps_gb300 import api
-        if args.only == "ring_allreduce":
+        api.lib()
+        peak = float(load_peaks()[0]["bf16_tflops"])
+        o = args.only
+        if o == "ring_allreduce":
             res = ring_results(api, torch, args.steps)
-        elif args.only == "alltoall":
+        elif o == "alltoall":
             res = alltoall_results(api, torch, args.steps)
-        elif args.only == "ag_tiny":
+        elif o == "ag_tiny":
             res = tiny_results(api, torch)
-        elif args.only.startswith("rs_"):
-            res = rs_results(api, torch, args.steps, scatter_only=args.only.endswith("_scatter"))
-        elif args.only.endswith("_gather"):
-            res = ag_fused_results(api, torch, args.only[:-len("_gather")], args.steps,
+        elif o == "tp_layer":
+            res = tp_layer_results(api, torch, peak, args.steps)
+        elif o == "rs_tp_all":
+            res = rs_config_results(api, torch, peak, args.steps)
+        elif o.endswith("_all"):
+            res = ag_config_results(api, torch, o[:-len("_all")], peak, args.steps)
+        elif o.startswith("rs_"):
+            res = rs_results(api, torch, args.steps, scatter_only=o.endswith("_scatter"))
+        elif o.endswith("_gather"):
+            res = ag_fused_results(api, torch, o[:-len("_gather")], args.steps,
                                    producer_only=True)
         else:
-            res = ag_fused_results(api, torch, args.only, args.steps)
-        print(json.dumps({args.only: res}), flush=True)
+            res = ag_fused_results(api, torch, o, args.steps)
+        print(json.dumps({o: res}), flush=True)
         return 0
     if world > 1:
         import torch

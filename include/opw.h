@@ -263,11 +263,9 @@ int64_t opw_ag_trace_words(int32_t R, int64_t M_r, int64_t N, int64_t K);
  * cta_group::2 MMAs with TMEM accumulators.  After the launch every flag slot
  * holds `epoch` and G is bit-identical to the concatenation.
  *
- * The kernel is launched cooperatively (every CTA resident at once, which the
- * flag waits between CTAs need).  ncu cannot profile a cooperative clustered
- * launch: with the environment variable OPW_AG_LAUNCH_NONCOOPERATIVE set when
- * the library is first used, the cooperative attribute is left out (the grid
- * is still sized to be resident) so the kernel can be captured.
+ * Producer warps claim flag tiles from a device counter in publish order, so
+ * every flag is published by CTAs that are running: the launch (clusters of 2,
+ * one CTA per SM) needs no co-residency guarantee, and profilers can replay it.
  *
  * Shapes: M_r, K multiples of 64 (flag tile 64) or 128; N a multiple of 8;
  * R*M_r, N, K <= 2^31.  Alignment: heap_dev, B_dev, G_dev, C_dev, a_off and
@@ -304,8 +302,14 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
  * therefore race and give wrong results: serialise them.
  *
  * Set-up: the first call on a device, with that device current, looks up
- * the array's device address.  Make that first call before any stream
- * capture.
+ * the array's device address and keeps it for the life of the process.  Make
+ * that first call before any stream capture.  cudaDeviceReset() (or anything
+ * else that destroys the device's primary context) invalidates the kept
+ * address: do not call this entry point on that device afterwards.
+ *
+ * Every buffer (the heap, B_dev, G_dev, C_dev, status_dev) must be memory of
+ * the current device; otherwise the call returns OPW_ERR_INVALID_ARG before
+ * launching anything.
  *
  *   status_dev : device int32[4], 16-byte aligned, written by the call:
  *                [0] status (OPW_OK or a device-side error such as

@@ -279,10 +279,18 @@ def ag_gemm_noalloc_status(heap, rank_off, a_off, M_r, N, K, B, G, C, status, op
     """opw_ag_gemm_noalloc, for callers that cannot allocate device memory.
 
     Same result as ag_gemm, with its scratch in a fixed array inside the
-    library instead of a signal object.  `status` is a caller-owned device
-    int32 tensor of 4 elements that receives the device-side status.
-    Returns the host-side status code.
+    library instead of a signal object.  `status` is a caller-owned int32
+    tensor of at least 4 contiguous elements on the current CUDA device (or
+    any object whose data_ptr() is such a device address); it receives the
+    device-side status.  Returns the host-side status code (ERR_INVALID_ARG
+    for a status tensor of the wrong kind).
     """
+    if isinstance(status, torch.Tensor):
+        # the library writes 4 int32 words there from the current device
+        if (not status.is_cuda or status.dtype != torch.int32 or status.numel() < 4
+                or not status.is_contiguous()
+                or status.device.index != torch.cuda.current_device()):
+            return ERR_INVALID_ARG
     s = _symm(heap, rank_off)
     return int(lib().opw_ag_gemm_noalloc(ctypes.byref(s), int(a_off), int(M_r), int(N), int(K),
                                          B.data_ptr(), G.data_ptr(), C.data_ptr(),

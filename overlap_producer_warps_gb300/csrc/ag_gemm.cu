@@ -19,9 +19,10 @@
 //   warp 1     MMA (even CTA only): one thread issues the pair's tcgen05.mma
 //              (bf16 x bf16 -> fp32) into a double-buffered TMEM accumulator
 //              (2 x 128 lanes x 256 columns in each CTA).
-//   warp 2     gather producer (every CTA): TMA-copies flag tiles of A_r into G
-//              through shared memory, waits for the copy to complete, and
-//              publishes the tile's flag with st.release.gpu.
+//   warp 2     gather producer (every CTA): claims flag tiles of A_r from a
+//              device counter in publish order, TMA-copies each into G through
+//              shared memory, waits for the copy to complete, and publishes the
+//              tile's flag with st.release.gpu.
 //   warp 3     allocates / frees the pair's TMEM; in the even CTA it is also
 //              the scheduler: it picks the next output tile, acquires
 //              (ld.acquire.gpu) the flags of all the A rows that tile needs
@@ -40,7 +41,6 @@
 // frees TMEM and returns.  Cluster barriers bracket the kernel, so neither CTA
 // of a pair leaves while the other may still use its shared memory or TMEM.
 #include <atomic>
-#include <cstdlib>
 
 #include "opw_device.cuh"
 #include "opw_kernels.h"
@@ -602,60 +602,149 @@ __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uin
 
 // ------------------------------------------------------------------ gather producer
 
+// Flag tile at position `pidx` of the publish order, and the position of its
+// rank in a permuted publish order (0 without one).
+struct GatherItem {
+    int r, mt, kt, ip;
+};
+
+__device__ __forceinline__ GatherItem gather_item(const AgParams& p, int pidx)
+{
+    const int per_rank = p.T_mr * p.T_k;
+    GatherItem g;
+    g.ip = 0;
+    if (p.has_perm) {
+        // rank-major in publish order
+        g.ip = pidx / per_rank;
+        g.r = p.perm[g.ip];
+        const int rem = pidx - g.ip * per_rank;
+        g.mt = rem / p.T_k;
+        g.kt = rem - g.mt * p.T_k;
+    } else {
+        // row block by row block, ranks interleaved, k fastest; the
+        // consumer's own rank (read in place) last
+        const int others = p.local_rank >= 0 ? (p.R - 1) * per_rank : p.R * per_rank;
+        if (pidx < others) {
+            const int Ro = p.local_rank >= 0 ? p.R - 1 : p.R;
+            g.mt = pidx / (Ro * p.T_k);
+            const int rem = pidx - g.mt * Ro * p.T_k;
+            const int ri = rem / p.T_k;
+            g.r = (p.local_rank >= 0 && ri >= p.local_rank) ? ri + 1 : ri;
+            g.kt = rem - ri * p.T_k;
+        } else {
+            const int j = pidx - others;
+            g.r = p.local_rank;
+            g.mt = j / p.T_k;
+            g.kt = j - g.mt * p.T_k;
+        }
+    }
+    return g;
+}
+
+// Lane 0: the tile's copy into G is complete (every bulk store committed so
+// far has been written), so publish its flag: SET the epoch with a release
+// (or, with batched signals, ADD 1 to its row counter), then count it in its
+// rank's publish counter.
+__device__ __forceinline__ void publish_tile(const AgParams& p, const ErrCtx& ec, const GatherItem& g)
+{
+    bulk_wait<0>();
+    fence_async_global();
+    const int slot = (g.r * p.T_mr + g.mt) * p.T_k + g.kt;
+    int64_t v = static_cast<int64_t>(p.epoch);
+    bool skip = false;
+    if (p.fault_kind == OPW_FAULT_DROP_TILE && slot == p.fault_arg) skip = true;
+    if (p.fault_kind == OPW_FAULT_STALE_EPOCH && slot == p.fault_arg) v -= 1;
+    // the publish time is read before the release, so no consumer can
+    // observe the flag earlier than the recorded time
+    const uint64_t t_pub = p.trace != nullptr ? globaltimer() : 0;
+    const bool checked = p.sync_mode == OPW_SYNC_CHECKED;
+    if (p.signal_mode == OPW_SIGNAL_ROW_ADD) {
+        // batched signal: one counter per flag row, +1 per k-tile
+        if (!skip && v == static_cast<int64_t>(p.epoch)) {
+            unsigned long long* ctr =
+                reinterpret_cast<unsigned long long*>(p.flags) + g.r * p.T_mr + g.mt;
+            if (checked) {
+                // this epoch's adds take the counter from (e-1)*T_k to e*T_k
+                const uint64_t old = atom_add_release(ctr, 1ull);
+                const uint64_t lo = (p.epoch - 1) * static_cast<uint64_t>(p.T_k);
+                if (old < lo || old >= lo + static_cast<uint64_t>(p.T_k))
+                    raise_error(ec, OPW_ERR_FLAG_PROTOCOL, g.r, g.r * p.T_mr + g.mt);
+            } else {
+                red_release_add(ctr, 1ull);
+            }
+        }
+    } else if (!skip) {
+        if (checked) {
+            if (atom_exch_release(p.flags + slot, v) != static_cast<int64_t>(p.epoch) - 1)
+                raise_error(ec, OPW_ERR_FLAG_PROTOCOL, g.r, slot);
+        } else {
+            st_release(p.flags + slot, v);
+        }
+    }
+    red_release_add(p.counters + CTR_RANK_DONE + g.r, 1ull);
+    if (p.trace != nullptr) p.trace[slot] = t_pub;
+}
+
+// Warp 2 of every CTA.  Flag tiles are claimed one at a time from a device
+// counter, in publish order, by whichever producer warps are running, so no
+// wait anywhere in the grid depends on a CTA that has not started: the launch
+// needs no co-residency guarantee.  A tile is copied 32 rows at a time: TMA
+// loads of A_r rows into the staging buffers, then a TMA store of each into G
+// as it lands.  The next tile's loads are issued before the previous tile's
+// stores are waited for and its flag published, and the next claim is made
+// while the current tile is in flight.
 __device__ void run_gather(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const ErrCtx& ec,
                            uint64_t t_start)
 {
     const uint32_t lane = lane_id();
-    const int G = static_cast<int>(gridDim.x);
-    const int c = static_cast<int>(blockIdx.x);
-    const int per_rank = p.T_mr * p.T_k;
-    const int n_items = p.R * per_rank;
-    const int subs = p.ft / GATHER_SUB_ROWS;
+    const int n_items = p.R * p.T_mr * p.T_k;
+    const int subs = p.ft / GATHER_SUB_ROWS;  // 2 or 4, at most GATHER_BUFS
     const uint32_t sub_bytes = static_cast<uint32_t>(p.ft) * GATHER_SUB_ROWS * 2u;
-    const int n_mine = c < n_items ? (n_items - c + G - 1) / G : 0;
     uint8_t* buf0 = smem + OFF_GATHER;
+    unsigned long long* claim_ctr = p.counters + CTR_GATHER;
+
+    auto claimed = [&](unsigned long long raw) -> int {
+        const long long v = static_cast<long long>(__shfl_sync(0xffffffffu, raw, 0) - p.gather_base);
+        return v < n_items ? static_cast<int>(v) : -1;
+    };
+    unsigned long long raw = 0;
+    if (lane == 0) raw = atomicAdd(claim_ctr, 1ull);
+    int cur = claimed(raw);
+
     int ordered_upto = 0;  // rank positions whose predecessors are known complete
-    uint32_t seq = 0;      // sub-box sequence number across this warp's flag tiles
+    uint32_t seq = 0;      // sub-box sequence number: buffer seq % GATHER_BUFS
+    bool pending = false;  // `pend` is copied (stores committed) but not yet published
+    GatherItem pend{0, 0, 0, 0};
     bool ok = true;
 
-    for (int it = 0; it < n_mine && ok; ++it) {
-        const int pidx = c + it * G;
-        int r, mt, kt, ip = 0;
-        if (p.has_perm) {
-            // rank-major in publish order
-            ip = pidx / per_rank;
-            r = p.perm[ip];
-            const int rem = pidx - ip * per_rank;
-            mt = rem / p.T_k;
-            kt = rem - mt * p.T_k;
-        } else {
-            // row block by row block, ranks interleaved, k fastest; the
-            // consumer's own rank (read in place) last
-            const int others = p.local_rank >= 0 ? (p.R - 1) * per_rank : n_items;
-            if (pidx < others) {
-                const int Ro = p.local_rank >= 0 ? p.R - 1 : p.R;
-                mt = pidx / (Ro * p.T_k);
-                const int rem = pidx - mt * Ro * p.T_k;
-                const int ri = rem / p.T_k;
-                r = (p.local_rank >= 0 && ri >= p.local_rank) ? ri + 1 : ri;
-                kt = rem - ri * p.T_k;
-            } else {
-                const int j = pidx - others;
-                r = p.local_rank;
-                mt = j / p.T_k;
-                kt = j - mt * p.T_k;
-            }
-        }
+    while (cur >= 0 && ok) {
+        const GatherItem g = gather_item(p, cur);
+        // the next claim travels while this tile is copied
+        raw = 0;
+        if (lane == 0) raw = atomicAdd(claim_ctr, 1ull);
 
-        // Skewed readiness: rank r starts no earlier than delay_ns[r] ...
+        // Skewed readiness: rank r starts no earlier than delay_ns[r] after
+        // this CTA started, and only after every tile of the rank published
+        // before it.  Never wait while holding an unpublished tile: it may be
+        // one the wait is for.
+        uint32_t need_delay = 0;
+        uint64_t d = 0;
         if (p.has_delay) {
-            const uint64_t d = p.delay_ns[r] < ec.timeout_ns ? p.delay_ns[r] : ec.timeout_ns;
-            while (globaltimer() - t_start < d) __nanosleep(256);
+            d = p.delay_ns[g.r] < ec.timeout_ns ? p.delay_ns[g.r] : ec.timeout_ns;
+            if (lane == 0) need_delay = globaltimer() - t_start < d ? 1u : 0u;
+            need_delay = __shfl_sync(0xffffffffu, need_delay, 0);
         }
-        // ... and only after every tile of the rank published before it.
-        if (p.has_perm && ip > 0 && ordered_upto < ip) {
-            const uint64_t target = p.rank_target[p.perm[ip - 1]];
-            const unsigned long long* ctr = p.counters + CTR_RANK_DONE + p.perm[ip - 1];
+        const bool need_order = p.has_perm && g.ip > 0 && ordered_upto < g.ip;
+        if ((need_delay || need_order) && pending) {
+            if (lane == 0) publish_tile(p, ec, pend);
+            __syncwarp();
+            pending = false;
+        }
+        if (need_delay)
+            while (globaltimer() - t_start < d) __nanosleep(256);
+        if (need_order) {
+            const uint64_t target = p.rank_target[p.perm[g.ip - 1]];
+            const unsigned long long* ctr = p.counters + CTR_RANK_DONE + p.perm[g.ip - 1];
             const uint64_t t0 = globaltimer();
             for (uint32_t s = 0;; ++s) {
                 uint32_t done = 0;
@@ -666,102 +755,66 @@ __device__ void run_gather(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
                 if ((s & 7u) == 7u) {
                     if (aborted(ec)) { ok = false; break; }
                     if (globaltimer() - t0 > ec.timeout_ns) {
-                        if (lane == 0) raise_error(ec, OPW_ERR_TIMEOUT, p.perm[ip - 1], SITE_SKEW_ORDER);
+                        if (lane == 0) raise_error(ec, OPW_ERR_TIMEOUT, p.perm[g.ip - 1], SITE_SKEW_ORDER);
                         ok = false;
                         break;
                     }
                 }
             }
             if (!ok) break;
-            ordered_upto = ip;
+            ordered_upto = g.ip;
         }
 
-        // Copy the flag tile 32 rows at a time through the staging buffers:
-        // TMA loads of A_r rows -> shared (up to GATHER_BUFS in flight), then
-        // a TMA store shared -> G as each one lands.  Sub-box number `sq`
-        // uses buffer sq % GATHER_BUFS for the (sq / GATHER_BUFS)-th time.
-        const int x = kt * p.ft;
-        const int y_src = mt * p.ft;
-        const int y_dst = r * p.M_r + mt * p.ft;
-        auto issue_load = [&](uint32_t sq, int sub) {
-            if (lane == 0) {
-                bulk_wait_read<0>();  // earlier stores are done reading the staging buffers
+        // Loads of this tile.  Its buffers were last read by the previous
+        // tile's stores: those must have finished reading shared memory.
+        const int x = g.kt * p.ft;
+        const int y_src = g.mt * p.ft;
+        const int y_dst = g.r * p.M_r + g.mt * p.ft;
+        if (lane == 0) {
+            bulk_wait_read<0>();
+            for (int sub = 0; sub < subs; ++sub) {
+                const uint32_t sq = seq + static_cast<uint32_t>(sub);
                 uint64_t* fb = &ctrl->gfull[sq % GATHER_BUFS];
                 mbar_arrive_expect_tx(fb, sub_bytes);
-                tma_load_2d(buf0 + (sq % GATHER_BUFS) * GATHER_BUF_BYTES, &p.shard[r], fb, x,
+                tma_load_2d(buf0 + (sq % GATHER_BUFS) * GATHER_BUF_BYTES, &p.shard[g.r], fb, x,
                             y_src + sub * GATHER_SUB_ROWS);
             }
+        }
+        __syncwarp();
+        // The previous tile's stores are the only ones committed: wait for
+        // them and publish it while this tile's loads are in flight.
+        if (pending) {
+            if (lane == 0) publish_tile(p, ec, pend);
             __syncwarp();
-        };
-        const int ahead = subs < GATHER_BUFS ? subs : GATHER_BUFS;
-        for (int sub = 0; sub < ahead; ++sub) issue_load(seq + sub, sub);
-        int issued = ahead;
+            pending = false;
+        }
+        // Store each sub-box into G as it lands.
         for (int sub = 0; sub < subs; ++sub) {
-            if (!wait_bar(&ctrl->gfull[seq % GATHER_BUFS], (seq / GATHER_BUFS) & 1u, ec,
+            const uint32_t sq = seq + static_cast<uint32_t>(sub);
+            if (!wait_bar(&ctrl->gfull[sq % GATHER_BUFS], (sq / GATHER_BUFS) & 1u, ec,
                           SITE_GATHER_LOAD)) {
                 // every outstanding load must land before the CTA may exit
-                for (int k = sub; k < issued; ++k) {
-                    const uint32_t sq = seq + (k - sub);
-                    drain_bar(&ctrl->gfull[sq % GATHER_BUFS], (sq / GATHER_BUFS) & 1u, ec);
+                for (int k = sub; k < subs; ++k) {
+                    const uint32_t sk = seq + static_cast<uint32_t>(k);
+                    drain_bar(&ctrl->gfull[sk % GATHER_BUFS], (sk / GATHER_BUFS) & 1u, ec);
                 }
                 ok = false;
                 break;
             }
             if (lane == 0) {
-                tma_store_2d(&p.g_store, buf0 + (seq % GATHER_BUFS) * GATHER_BUF_BYTES, x,
+                tma_store_2d(&p.g_store, buf0 + (sq % GATHER_BUFS) * GATHER_BUF_BYTES, x,
                              y_dst + sub * GATHER_SUB_ROWS);
                 bulk_commit();
             }
             __syncwarp();
-            ++seq;
-            if (issued < subs) {
-                issue_load(seq + (issued - sub - 1), issued);
-                ++issued;
-            }
         }
         if (!ok) break;
-
-        // Publish: the copy is complete, then release the flag (SET epoch).
-        if (lane == 0) {
-            bulk_wait<0>();
-            fence_async_global();
-            const int slot = (r * p.T_mr + mt) * p.T_k + kt;
-            int64_t v = static_cast<int64_t>(p.epoch);
-            bool skip = false;
-            if (p.fault_kind == OPW_FAULT_DROP_TILE && slot == p.fault_arg) skip = true;
-            if (p.fault_kind == OPW_FAULT_STALE_EPOCH && slot == p.fault_arg) v -= 1;
-            // the publish time is read before the release, so no consumer can
-            // observe the flag earlier than the recorded time
-            const uint64_t t_pub = p.trace != nullptr ? globaltimer() : 0;
-            const bool checked = p.sync_mode == OPW_SYNC_CHECKED;
-            if (p.signal_mode == OPW_SIGNAL_ROW_ADD) {
-                // batched signal: one counter per flag row, +1 per k-tile
-                if (!skip && v == static_cast<int64_t>(p.epoch)) {
-                    unsigned long long* ctr =
-                        reinterpret_cast<unsigned long long*>(p.flags) + r * p.T_mr + mt;
-                    if (checked) {
-                        // this epoch's adds take the counter from (e-1)*T_k to e*T_k
-                        const uint64_t old = atom_add_release(ctr, 1ull);
-                        const uint64_t lo = (p.epoch - 1) * static_cast<uint64_t>(p.T_k);
-                        if (old < lo || old >= lo + static_cast<uint64_t>(p.T_k))
-                            raise_error(ec, OPW_ERR_FLAG_PROTOCOL, r, r * p.T_mr + mt);
-                    } else {
-                        red_release_add(ctr, 1ull);
-                    }
-                }
-            } else if (!skip) {
-                if (checked) {
-                    if (atom_exch_release(p.flags + slot, v) != static_cast<int64_t>(p.epoch) - 1)
-                        raise_error(ec, OPW_ERR_FLAG_PROTOCOL, r, slot);
-                } else {
-                    st_release(p.flags + slot, v);
-                }
-            }
-            red_release_add(p.counters + CTR_RANK_DONE + r, 1ull);
-            if (p.trace != nullptr) p.trace[slot] = t_pub;
-        }
-        __syncwarp();
+        seq += static_cast<uint32_t>(subs);
+        pending = true;
+        pend = g;
+        cur = claimed(raw);
     }
+    if (pending && ok && lane == 0) publish_tile(p, ec, pend);
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
 }
@@ -856,20 +909,15 @@ cudaLaunchConfig_t pair_config(unsigned pairs, cudaStream_t s, cudaLaunchAttribu
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = SMEM_ALLOC;
     cfg.stream = s;
+    // Clusters of 2 only.  No cross-CTA wait depends on a CTA that has not
+    // started (producers claim flag tiles dynamically; consumers wait only on
+    // flags), so the launch needs no co-residency guarantee.
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    // Consumers wait on flags that other CTAs' producers publish: every CTA
-    // must be resident at once.  The cooperative attribute guarantees it.
-    // ncu cannot launch a kernel that is both cooperative and clustered, so
-    // OPW_AG_LAUNCH_NONCOOPERATIVE=1 leaves the attribute out for profiling;
-    // the grid, sized by the cluster occupancy query, still fits the GPU.
-    static const bool coop = std::getenv("OPW_AG_LAUNCH_NONCOOPERATIVE") == nullptr;
-    attr[1].id = cudaLaunchAttributeCooperative;
-    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = coop ? 2 : 1;
+    cfg.numAttrs = 1;
     return cfg;
 }
 
@@ -900,9 +948,8 @@ int ag_max_pairs()
     if (!set_smem_attr()) return 0;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config(static_cast<unsigned>(sms / 2), nullptr, attr);
-    cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pair_config(static_cast<unsigned>(sms / 2), nullptr, attr);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, ag_gemm_kernel, &cfg) != cudaSuccess) return 0;
     cached[dev] = n;
@@ -912,7 +959,7 @@ int ag_max_pairs()
 cudaError_t launch_ag_gemm(const AgParams& p, int pairs, cudaStream_t s)
 {
     if (!set_smem_attr()) return cudaErrorInvalidDevice;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = pair_config(static_cast<unsigned>(pairs), s, attr);
     return cudaLaunchKernelEx(&cfg, ag_gemm_kernel, p);
 }

@@ -56,6 +56,18 @@ cudaError_t scratch_for_device(int dev, void** out)
     return cudaSuccess;
 }
 
+// True if `ptr` is device (or managed) memory that device `dev` owns.  A
+// failed query leaves no error pending for the caller's next CUDA call.
+bool on_device(const void* ptr, int dev)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) && a.device == dev;
+}
+
 // Every call starts from zero: flags, counters and the caller's status word.
 __global__ void noalloc_clear_kernel(int64_t* flags, int64_t n_flags, unsigned long long* counters,
                                      int32_t* status)
@@ -96,6 +108,11 @@ extern "C" opw_status opw_ag_gemm_noalloc(const opw_symm* symm, size_t a_off, in
     // ---- set-up for this device (first call only), then the launches
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return OPW_ERR_CUDA;
+    // The kernels run with this device's scratch: every buffer must be this
+    // device's memory too.
+    if (!on_device(status_dev, dev) || !on_device(symm->heap_dev, dev) || !on_device(B_dev, dev) ||
+        !on_device(G_dev, dev) || !on_device(C_dev, dev))
+        return OPW_ERR_INVALID_ARG;
     void* scratch = nullptr;
     if (scratch_for_device(dev, &scratch) != cudaSuccess) return OPW_ERR_CUDA;
     const int pairs = ag_pairs_for(o, dev);
@@ -111,6 +128,7 @@ extern "C" opw_status opw_ag_gemm_noalloc(const opw_symm* symm, size_t a_off, in
     p.counters = counters;
     p.epoch = 1;  // flags were just cleared to 0
     p.claim_base = 0;
+    p.gather_base = 0;
     for (int i = 0; i < R; ++i) p.rank_target[i] = static_cast<uint64_t>(p.T_mr) * p.T_k;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);

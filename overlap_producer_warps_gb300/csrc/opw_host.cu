@@ -1,6 +1,6 @@
 // Host side of the C ABI declared in include/opw.h: argument validation,
 // signal objects (flags, epochs, status word, counters), tensor-map
-// encoding and the cooperative launches.  Nothing here prints, throws or
+// encoding and the launches.  Nothing here prints, throws or
 // allocates except opw_signal_alloc.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -43,6 +43,7 @@ opw_status reset_device(opw_signal* s, cudaStream_t st)
     s->epoch_last = 0;
     for (int r = 0; r < OPW_MAX_RANKS; ++r) s->rank_done[r] = s->rank_target_last[r] = 0;
     s->claim_next = 0;
+    s->gather_next = 0;
     s->latched = false;
     s->mode = -1;
     s->mode_tk = 0;
@@ -407,6 +408,7 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
     p.counters = sig->counters;
     p.epoch = epoch;
     p.claim_base = sig->claim_next;
+    p.gather_base = sig->gather_next;
     const uint64_t per_rank = static_cast<uint64_t>(p.T_mr) * p.T_k;
     for (int r = 0; r < R; ++r)
         p.rank_target[r] = produces ? sig->rank_done[r] + per_rank : sig->rank_target_last[r];
@@ -419,6 +421,9 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
     sig->mode_tk = K / ft;
     if (produces) {
         sig->epoch_last = epoch;
+        // every flag tile is claimed once, and every CTA's producer makes one
+        // claim past the end
+        sig->gather_next += per_rank * static_cast<uint64_t>(R) + 2u * static_cast<uint64_t>(pairs);
         for (int r = 0; r < R; ++r) {
             sig->rank_target_last[r] = p.rank_target[r];
             sig->rank_done[r] = p.rank_target[r];

@@ -27,9 +27,11 @@ constexpr int GATHER_SUB_ROWS = 32;              // producer copies a flag tile 
 constexpr int GATHER_BUF_BYTES = GATHER_SUB_ROWS * 128 * 2;  // 8 KiB (flag tile <= 128 wide)
 
 // Counter words in the signal object after the flags: per-rank publish
-// counts, then the tile-claim counter of the dynamic schedule.
+// counts, the tile-claim counter of the dynamic consumer schedule, and the
+// flag-tile claim counter of the producer warps.
 constexpr int CTR_RANK_DONE = 0;
 constexpr int CTR_CLAIM = OPW_MAX_RANKS;
+constexpr int CTR_GATHER = OPW_MAX_RANKS + 1;
 constexpr int CTR_WORDS = OPW_MAX_RANKS + 8;
 
 // Error-site tags written to status[2] when an on-chip wait times out.
@@ -59,6 +61,7 @@ struct AgParams {
     uint64_t epoch;
     uint64_t timeout_ns;
     uint64_t claim_base;      // claim-counter value before this launch
+    uint64_t gather_base;     // producer claim-counter value before this launch
     int32_t R, M_r, M, N, K;
     int32_t ft;               // flag tile edge (64 or 128)
     int32_t T_mr, T_k;        // flag tiles per rank along M, along K
@@ -109,7 +112,6 @@ constexpr int RING_PIECE = 1024;  // fp32 values one warp moves per ring action
 size_t ag_smem_bytes();
 size_t rs_smem_bytes();
 
-// Launch helpers (cooperative launch so every CTA is co-resident).
 int ag_max_pairs();  // clusters of 2 AG-GEMM CTAs that fit at once (0 on error)
 
 // AG-GEMM host set-up shared by the two entry points (opw_host.cu).
@@ -144,6 +146,7 @@ struct opw_signal {
     uint64_t rank_done[OPW_MAX_RANKS];       // expected rank counters after all enqueued launches
     uint64_t rank_target_last[OPW_MAX_RANKS];  // targets of the last producing launch
     uint64_t claim_next;           // claim counter value after all enqueued launches
+    uint64_t gather_next;          // producer claim counter value after all enqueued launches
     bool latched;                  // opw_status_sync saw a device error
     int32_t mode;                  // signal mode since the last reset (-1: none yet)
     int64_t mode_tk;               // K/ft used with OPW_SIGNAL_ROW_ADD since the last reset

@@ -120,3 +120,12 @@ def sample_rows(M: int, tile: int, per_tile: int, seed: int) -> np.ndarray:
         rows.update([t0, t1 - 1])
         rows.update(rng.integers(t0, t1, size=per_tile).tolist())
     return np.array(sorted(rows), dtype=np.int64)
+
+
+def quarter_rows(M: int, seed: int) -> np.ndarray:
+    """One random row from each 32-row quarter of every 128-row block: every
+    epilogue warp of both CTAs of every pair tile writes one of them."""
+    rng = np.random.default_rng(seed)
+    base = np.arange(0, M, 32, dtype=np.int64)
+    rows = base + rng.integers(0, 32, size=base.size)
+    return np.minimum(rows, M - 1)

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from overlap_producer_warps_gb300 import inputs
-from tests.helpers import AgProblem, assert_gemm_close, host_bits, sample_rows
+from tests.helpers import AgProblem, assert_gemm_close, host_bits, quarter_rows, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -287,8 +287,10 @@ def test_full_size_configs_sampled(api, name):
     G = host_bits(prob.G)
     assert np.array_equal(G, oracle.allgather(d["heap"], d["rank_off"], prob.R, d["a_off"],
                                               prob.M_r, prob.K))
-    per_tile = 1 if prob.M * prob.N * prob.K < 2 ** 38 else 0
-    rows = sample_rows(prob.M, 128 if per_tile else 512, per_tile, seed=1)
+    # one row in every 32-row quarter of every 128-row block: each epilogue
+    # warp of both CTAs of every pair tile, in every column tile
+    rows = quarter_rows(prob.M, seed=1)
+    assert len(rows) == prob.M // 32
     C = host_bits(prob.C)
     assert_gemm_close(C[rows], prob.oracle_rows(rows), what=f"{name} sampled C")
 
