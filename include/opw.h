@@ -360,12 +360,38 @@ int64_t opw_rs_num_flags(int32_t R, int64_t M, int64_t N);
  * Shapes: M a multiple of 128*R; K_r and N multiples of 8 (a ragged last
  * k-block or column tile is zero-filled by TMA and not stored).
  * Alignment and errors as for opw_ag_gemm.  `opts` fields used: timeout_ns,
- * num_ctas, role, sync_mode (OVERLAP or CHECKED); the others must be
- * defaults.
+ * num_ctas, role, sync_mode (OVERLAP or CHECKED), trace_dev, fault_kind
+ * (NONE, or DROP_TILE: flag slot fault_arg is never published); the others
+ * must be defaults.  With trace_dev (device, 2 * opw_rs_num_flags() uint64
+ * words) word `slot` receives the %globaltimer time at which the slot was
+ * published, and word F + slot the time the receiving side of
+ * opw_gemm_rs_consume acquired it.
  */
 opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t out_off,
                        int64_t M, int64_t N, int64_t K_r, opw_signal* sig, uint64_t epoch,
                        const opw_opts* opts, void* stream);
+
+/*
+ * GEMM -> ReduceScatter with the receiving side in the same launch
+ * ("GEMM and ReduceScatter Overlapping", step 3: the consumer waits for
+ * tiles as they are published).  Computes exactly what opw_gemm_rs computes,
+ * and in addition, for every 128x128 output tile of every rank's block, a
+ * warp on another SM than the one that stored the tile acquires the tile's
+ * flag (>= epoch, a bounded wait) and only then copies the tile from out_j
+ * into recv_dev.  Afterwards recv_dev [M, N] bf16 (row i of S at row i)
+ * equals the concatenation out_0, ..., out_{R-1} bit for bit.
+ *
+ *   recv_dev : device, [M, N] bf16, 16-byte aligned, must not overlap the
+ *              heap's A_r, B_r or out_j; written only after each tile's flag
+ *              is acquired.
+ * opts->role must be OPW_ROLE_FUSED.  A flag that never comes (fault_kind
+ * DROP_TILE) makes the receiving wait run out: OPW_ERR_TIMEOUT with the
+ * rank and slot, latched in the signal object.  Other arguments and errors
+ * as for opw_gemm_rs; recv_dev NULL is INVALID_ARG.
+ */
+opw_status opw_gemm_rs_consume(const opw_symm* symm, size_t a_off, size_t b_off, size_t out_off,
+                               int64_t M, int64_t N, int64_t K_r, void* recv_dev, opw_signal* sig,
+                               uint64_t epoch, const opw_opts* opts, void* stream);
 
 /* ---------------------------------------------------------- ring AllReduce */
 

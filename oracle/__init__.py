@@ -99,9 +99,7 @@ def _load():
             "opw_oracle_alltoall": (None, [_u8p, _i64p, ctypes.c_int, ctypes.c_int64,
                                            ctypes.c_int64, ctypes.c_int64, _u8p]),
             "opw_oracle_swizzle_row": (ctypes.c_int64, [ctypes.c_int64] * 4),
-            "opw_oracle_consumer_order": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64,
-                                                           ctypes.c_int, ctypes.c_int64,
-                                                           ctypes.c_int64, _i64p]),
+            "opw_oracle_consumer_order": (ctypes.c_int64, [ctypes.c_int64] * 7 + [_i64p, _i64p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -244,11 +242,15 @@ def swizzle_row(pid_m: int, rank: int, tiles_per_pe: int, total_tiles: int) -> i
     return int(_load().opw_oracle_swizzle_row(pid_m, rank, tiles_per_pe, total_tiles))
 
 
-def consumer_order(T_M: int, T_N: int, R: int, G: int, c: int) -> np.ndarray:
-    """Visit order (tile indices q = m*T_N + n) of consumer CTA c."""
+def consumer_order(T_M: int, T_N: int, G: int, c: int, group_rows: int, rank: int,
+                   tiles_per_pe: int, visit=None) -> np.ndarray:
+    """Visit order (tile indices q = m*T_N + n) of consumer c of rank `rank`;
+    `visit` (optional) lists the ranks in the order their rows are taken."""
     T = T_M * T_N
     out = np.empty(max(1, (T + G - 1) // G), dtype=np.int64)
-    n = _load().opw_oracle_consumer_order(T_M, T_N, R, G, c, _p(out, _i64p))
+    v = None if visit is None else np.ascontiguousarray(np.asarray(visit, dtype=np.int64))
+    n = _load().opw_oracle_consumer_order(T_M, T_N, G, c, group_rows, rank, tiles_per_pe,
+                                          None if v is None else _p(v, _i64p), _p(out, _i64p))
     return out[:n].copy()
 
 

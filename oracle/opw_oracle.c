@@ -363,27 +363,37 @@ int64_t opw_oracle_swizzle_row(int64_t pid_m, int64_t rank, int64_t tiles_per_pe
 }
 
 /*
- * The consumer schedule built on it.  The output has T_M row tiles and T_N
- * column tiles; logical rank r owns row tiles [r*T_M/R, (r+1)*T_M/R), so
- * tiles_per_pe = T_M/R.  A persistent grid of G consumer CTAs shares the
- * T_M*T_N output tiles: tile q = m*T_N + n belongs to CTA q mod G.  CTA c
- * plays home rank h = c mod R and walks the row tiles in the swizzled order
- * m = swizzle_row(p, h, tiles_per_pe, T_M) for p = 0, 1, ..., T_M-1, taking
- * within each row the column tiles it owns in increasing n.  Writes CTA c's
- * tile indices in visit order to out and returns how many there are.
+ * The consumer schedule built on it.  The GPU plays one PE, rank `rank`, and
+ * computes all T_M x T_N output tiles (T_M row tiles, T_N column tiles) with
+ * a persistent grid of G consumers.  Every consumer follows one order of the
+ * tiles: row tiles in groups of group_rows consecutive rows, the column index
+ * outermost inside a group (so consumers working at the same time share the
+ * column tiles of B), and every row tile pid_m renamed so that the PE starts
+ * on its own rows and then moves on to the other ranks' rows.  With visit ==
+ * NULL the renaming is the page's formula swizzle_row(pid_m, rank,
+ * tiles_per_pe, T_M): rank+1's rows next, then rank+2's, ... (the order a
+ * ring delivers them).  Otherwise visit[k] names the rank whose rows come
+ * k-th (the PE's own rank first, then the others in the order they arrive):
+ * pid_m -> visit[pid_m / tiles_per_pe] * tiles_per_pe + pid_m % tiles_per_pe.
+ * Consumer c takes positions c, c+G, c+2G, ... of that order.  Writes
+ * consumer c's tile indices (q = m*T_N + n) in visit order to out and
+ * returns how many.
  */
-int64_t opw_oracle_consumer_order(int64_t T_M, int64_t T_N, int R, int64_t G, int64_t c,
-                                  int64_t* out)
+int64_t opw_oracle_consumer_order(int64_t T_M, int64_t T_N, int64_t G, int64_t c,
+                                  int64_t group_rows, int64_t rank, int64_t tiles_per_pe,
+                                  const int64_t* visit, int64_t* out)
 {
-    const int64_t tiles_per_pe = T_M / R;
-    const int64_t h = c % R;
     int64_t count = 0;
-    for (int64_t p = 0; p < T_M; ++p) {
-        const int64_t m = opw_oracle_swizzle_row(p, h, tiles_per_pe, T_M);
-        for (int64_t n = 0; n < T_N; ++n) {
-            const int64_t q = m * T_N + n;
-            if (q % G == c) out[count++] = q;
-        }
+    for (int64_t pos = c; pos < T_M * T_N; pos += G) {
+        const int64_t first = (pos / (group_rows * T_N)) * group_rows;  /* group's first row */
+        const int64_t rows = T_M - first < group_rows ? T_M - first : group_rows;
+        const int64_t local = pos - first * T_N;
+        const int64_t pid_m = first + local % rows;
+        const int64_t pid_n = local / rows;
+        const int64_t m = visit == NULL
+                              ? opw_oracle_swizzle_row(pid_m, rank, tiles_per_pe, T_M)
+                              : visit[pid_m / tiles_per_pe] * tiles_per_pe + pid_m % tiles_per_pe;
+        out[count++] = m * T_N + pid_n;
     }
     return count;
 }

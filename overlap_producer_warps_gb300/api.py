@@ -92,6 +92,10 @@ SIGNATURES = {
                                      ctypes.c_size_t, ctypes.c_int64, ctypes.c_int64,
                                      ctypes.c_int64, _vp, ctypes.c_uint64, ctypes.POINTER(Opts),
                                      _vp]),
+    "opw_gemm_rs_consume": (ctypes.c_int32, [ctypes.POINTER(Symm), ctypes.c_size_t,
+                                             ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int64,
+                                             ctypes.c_int64, ctypes.c_int64, _vp, _vp,
+                                             ctypes.c_uint64, ctypes.POINTER(Opts), _vp]),
 }
 
 _lock = threading.Lock()
@@ -313,6 +317,27 @@ def gemm_rs(heap, rank_off, a_off, b_off, out_off, M, N, K_r, sig: Signal, epoch
     """GEMM -> ReduceScatter (see opw_gemm_rs).  Asynchronous on `stream`."""
     _check(gemm_rs_status(heap, rank_off, a_off, b_off, out_off, M, N, K_r, sig, epoch, opts,
                           stream), "opw_gemm_rs")
+
+
+def gemm_rs_consume_status(heap, rank_off, a_off, b_off, out_off, M, N, K_r, recv,
+                           sig: Signal, epoch, opts=None, stream=None) -> int:
+    """opw_gemm_rs_consume, returning the raw status code."""
+    s = _symm(heap, rank_off)
+    return int(lib().opw_gemm_rs_consume(ctypes.byref(s), int(a_off), int(b_off), int(out_off),
+                                         int(M), int(N), int(K_r),
+                                         recv.data_ptr() if recv is not None else None,
+                                         sig.handle, int(epoch),
+                                         ctypes.byref(opts) if opts is not None else None,
+                                         _stream_ptr(stream)))
+
+
+def gemm_rs_consume(heap, rank_off, a_off, b_off, out_off, M, N, K_r, recv, sig: Signal, epoch,
+                    opts=None, stream=None):
+    """GEMM -> ReduceScatter with the receiving side in the same launch (see
+    opw_gemm_rs_consume): `recv` ([M, N] bf16) gets every rank's block after
+    its flags are acquired on the device.  Asynchronous on `stream`."""
+    _check(gemm_rs_consume_status(heap, rank_off, a_off, b_off, out_off, M, N, K_r, recv, sig,
+                                  epoch, opts, stream), "opw_gemm_rs_consume")
 
 
 def ring_num_flags(R: int, n: int) -> int:

@@ -116,50 +116,25 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, const 
     }
 }
 
-// Pair tile visited at position `idx` of the dynamic schedule.  Rows of pair
-// tiles (256 rows) are taken in the order their flag tiles are published, in
-// groups of p.group_rows rows; within a group the column index runs slowest,
-// so when B is larger than L2 can hold next to everything else, the pairs
-// working at the same time share B column tiles instead of streaming all of B
-// for every few rows (group_rows = 1 when B fits).
-__device__ __forceinline__ int ready_tile(const AgParams& p, int idx)
+// Pair tile at position `pos` of the consumers' tile order, which both
+// schedules share ("Threadblock Swizzling": the PE starts on its own rows;
+// "by the time a PE needs remote data, it's likely already transferred").
+// Pair rows are taken in groups of p.group_rows; within a group the column
+// index runs slowest, so when B is larger than L2 can hold next to
+// everything else, the pairs working at the same time share B column tiles
+// (group_rows = 1 when B fits).  Row position mp is renamed through the rank
+// visit order p.visit: the consumer's own rank first (read in place, no
+// wait), then every other rank in the order its tiles are published.  With
+// ranks published in ring order that renaming is the page's
+// pid_m -> (pid_m + rank * tiles_per_pe) mod total_tiles.
+__device__ __forceinline__ int ordered_tile(const AgParams& p, int pos)
 {
-    const int GM = p.group_rows;
-    const int group = idx / (GM * p.T_N);
-    const int first = group * GM;
-    const int rows = min(GM, p.T_M - first);
-    const int local = idx - first * p.T_N;
+    const int first = (pos / (p.group_rows * p.T_N)) * p.group_rows;
+    const int rows = min(p.group_rows, p.T_M - first);
+    const int local = pos - first * p.T_N;
     const int mp = first + local % rows;
     const int n = local / rows;
-    int m = mp;
-    if (p.ft == BM && p.M_r % PAIR_M == 0) {
-        const int tpr = p.M_r / PAIR_M;
-        if (p.local_rank >= 0 && p.R > 1) {
-            // the local rank's rows first (no wait), then the others in publish order
-            if (mp < tpr) {
-                m = p.local_rank * tpr + mp;
-            } else {
-                const int j = mp - tpr;
-                if (p.has_perm) {
-                    int ip = j / tpr;  // position among the other ranks in publish order
-                    int r = -1;
-                    for (int i = 0, seen = 0; i < p.R; ++i)
-                        if (p.perm[i] != p.local_rank) {
-                            if (seen == ip) { r = p.perm[i]; break; }
-                            ++seen;
-                        }
-                    m = r * tpr + j % tpr;
-                } else {
-                    const int k = j / (p.R - 1), ri = j % (p.R - 1);
-                    m = (ri < p.local_rank ? ri : ri + 1) * tpr + k;
-                }
-            }
-        } else if (p.has_perm) {
-            m = p.perm[mp / tpr] * tpr + mp % tpr;
-        } else {
-            m = (mp % p.R) * tpr + mp / p.R;
-        }
-    }
+    const int m = p.tpr > 0 ? p.visit[mp / p.tpr] * p.tpr + mp % p.tpr : mp;
     return m * p.T_N + n;
 }
 
@@ -378,13 +353,8 @@ __device__ void run_scheduler(const AgParams& p, AgCtrl* ctrl, const ErrCtx& ec)
     const int c = static_cast<int>(cluster_id_x());
     const int T = p.T_M * p.T_N;
 
-    // Static schedule: this pair owns tiles q = c + i*G; it starts at the first
-    // one in its home rank's rows (h*tiles_per_pe row tiles down) and wraps.
-    const int n_mine = c < T ? (T - c + G - 1) / G : 0;
-    const int h = c % p.R;
-    const long long start_q = static_cast<long long>(h) * (p.T_M / p.R) * p.T_N;
-    int i0 = start_q <= c ? 0 : static_cast<int>((start_q - c + G - 1) / G);
-    if (i0 >= n_mine) i0 = 0;
+    // Static schedule: pair c takes positions c, c + G, c + 2G, ... of the
+    // tile order; the dynamic one claims positions from a device counter.
 
     const uint32_t peer_tq_full0 = mapa_shared(smem_u32(&ctrl->tq_full[0]), 1);
     const uint32_t peer_tile_q0 = mapa_shared(smem_u32(&ctrl->tile_q[0]), 1);
@@ -403,9 +373,10 @@ __device__ void run_scheduler(const AgParams& p, AgCtrl* ctrl, const ErrCtx& ec)
             if (lane == 0)
                 idx = static_cast<long long>(atomicAdd(p.counters + CTR_CLAIM, 1ull) - p.claim_base);
             idx = __shfl_sync(0xffffffffu, idx, 0);
-            q = idx < T ? ready_tile(p, static_cast<int>(idx)) : -1;
+            q = idx < T ? ordered_tile(p, static_cast<int>(idx)) : -1;
         } else {
-            q = s < n_mine ? c + ((i0 + s) % n_mine) * G : -1;
+            const long long pos = c + static_cast<long long>(s) * G;
+            q = pos < T ? ordered_tile(p, static_cast<int>(pos)) : -1;
         }
         if (q >= 0) {
             if (p.trace != nullptr && lane == 0) {
@@ -621,16 +592,17 @@ __device__ __forceinline__ GatherItem gather_item(const AgParams& p, int pidx)
         g.mt = rem / p.T_k;
         g.kt = rem - g.mt * p.T_k;
     } else {
-        // row block by row block, ranks interleaved, k fastest; the
-        // consumer's own rank (read in place) last
+        // rank by rank in ring order after the consumer's own rank (the order
+        // a ring AllGather delivers them, and the order the swizzled consumers
+        // visit them), row block by row block, k fastest; the consumer's own
+        // rank (read in place) last
         const int others = p.local_rank >= 0 ? (p.R - 1) * per_rank : p.R * per_rank;
         if (pidx < others) {
-            const int Ro = p.local_rank >= 0 ? p.R - 1 : p.R;
-            g.mt = pidx / (Ro * p.T_k);
-            const int rem = pidx - g.mt * Ro * p.T_k;
-            const int ri = rem / p.T_k;
-            g.r = (p.local_rank >= 0 && ri >= p.local_rank) ? ri + 1 : ri;
-            g.kt = rem - ri * p.T_k;
+            const int ip = pidx / per_rank;
+            g.r = p.local_rank >= 0 ? (p.local_rank + 1 + ip) % p.R : ip;
+            const int rem = pidx - ip * per_rank;
+            g.mt = rem / p.T_k;
+            g.kt = rem - g.mt * p.T_k;
         } else {
             const int j = pidx - others;
             g.r = p.local_rank;

@@ -24,7 +24,12 @@
 //               rank's partial P_r = A_r * B_r goes into a fresh fp32 TMEM
 //               accumulator, alternating between two 256-column buffers.
 //   warp 2      allocates / frees the pair's TMEM.
-//   warp 3      idle.
+//   warp 3      the receiving side, when the caller asks for it (recv != NULL):
+//               for each pair tile it acquires the flags of the OTHER CTA's
+//               rows ("consumer waits for tiles", step 3) and copies each
+//               finished 128x128 tile from its rank's block into recv.  The
+//               other CTA runs on another SM, so every copy reads data that a
+//               different SM's TMA stores wrote and released.  Otherwise idle.
 //   warps 4-11  reduction (both CTAs): warp w reads TMEM lanes 32*(w&3).. and
 //               columns 128*((w-4)>>2)..+127 of each partial and adds it into a
 //               running fp32 sum held in registers, in rank order 0..R-1
@@ -108,11 +113,24 @@ __device__ __forceinline__ bool red_bar_and(bool v)
     return r != 0;
 }
 
-// Pair tiles of this cluster: q = cid + i * nc (256-row tiles of the full M,
-// 256 columns), the same sequence in both CTAs.
+// Pair tiles of this cluster: positions cid + i * nc of the tile order, the
+// same sequence in both CTAs.
 struct PairSched {
     int cid, nc, nt;
 };
+
+// The pair tile (row tile m, column tile n; 256 x 256) at position `pos` of
+// the tile order: pair rows in groups of p.group_rows, the column index
+// outermost inside a group, so that the pairs working at the same time read
+// fewer distinct B_r column tiles.
+__device__ __forceinline__ void rs_tile(const RsParams& p, int pos, int& m, int& n)
+{
+    const int first = (pos / (p.group_rows * p.T_N)) * p.group_rows;
+    const int rows = min(p.group_rows, p.T_M - first);
+    const int local = pos - first * p.T_N;
+    m = first + local % rows;
+    n = local / rows;
+}
 
 __device__ __forceinline__ PairSched pair_sched(const RsParams& p)
 {
@@ -134,9 +152,10 @@ __device__ void rs_loader(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, const 
     uint32_t stage = 0, sphase = 0, filled = 0, last_par = 0;
     bool ok = true;
     for (int i = 0; i < ps.nt && ok; ++i) {
-        const int q = ps.cid + i * ps.nc;
-        const int m0 = (q / p.T_N) * PAIR_M + static_cast<int>(crank) * BM;
-        const int n0 = (q % p.T_N) * BN + static_cast<int>(crank) * HALF_N;
+        int tm, tn;
+        rs_tile(p, ps.cid + i * ps.nc, tm, tn);
+        const int m0 = tm * PAIR_M + static_cast<int>(crank) * BM;
+        const int n0 = tn * BN + static_cast<int>(crank) * HALF_N;
         for (int r = 0; r < p.R && ok; ++r) {
             for (int kb = 0; kb < KB; ++kb) {
                 if (!wait_bar(&ctrl->empty[stage], sphase ^ 1u, ec, SITE_LOADER_EMPTY)) { ok = false; break; }
@@ -234,9 +253,10 @@ __device__ void rs_reduce(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32
     const bool scatter = p.role != OPW_ROLE_PRODUCER;
     for (int i = 0; i < ps.nt; ++i) {
         bool ok = true;
-        const int q = ps.cid + i * ps.nc;
-        const int m0 = (q / p.T_N) * PAIR_M + static_cast<int>(crank) * BM;
-        const int n0 = (q % p.T_N) * BN;
+        int tm, tn;
+        rs_tile(p, ps.cid + i * ps.nc, tm, tn);
+        const int m0 = tm * PAIR_M + static_cast<int>(crank) * BM;
+        const int n0 = tn * BN;
         float S[128];
 #pragma unroll
         for (int e = 0; e < 128; ++e) S[e] = 0.0f;
@@ -299,6 +319,7 @@ __device__ void rs_reduce(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32
                 const int ntile = n0 / 128 + t;
                 if (ntile < p.T_fn) {
                     const int slot = (j * p.T_fm + mt) * p.T_fn + ntile;
+                    if (p.fault_kind == OPW_FAULT_DROP_TILE && slot == p.fault_arg) continue;
                     const uint64_t t_pub = p.trace != nullptr ? globaltimer() : 0;
                     if (p.checked) {
                         if (atom_exch_release(p.flags + slot, static_cast<int64_t>(p.epoch)) !=
@@ -314,6 +335,60 @@ __device__ void rs_reduce(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32
     }
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
+}
+
+// Warp 3 of both CTAs, when recv is given: the receiving ranks' side.  For
+// each pair tile, in the pair's order, acquire (bounded, >= epoch) the flag of
+// each 128x128 output tile that the OTHER CTA of the pair reduced and stored,
+// then copy that tile from its rank's block out_j into recv (rows as in S).
+// Every lane acquires the flag itself, so each lane's loads are ordered after
+// it; the writer made its TMA stores visible (bulk wait, proxy fence) before
+// its release.
+__device__ void rs_receive(const RsParams& p, const ErrCtx& ec, uint32_t crank)
+{
+    if (p.recv == nullptr) return;
+    const uint32_t lane = lane_id();
+    const PairSched ps = pair_sched(p);
+    const int F = p.R * p.T_fm * p.T_fn;
+    const int64_t e = static_cast<int64_t>(p.epoch);
+    for (int i = 0; i < ps.nt; ++i) {
+        int tm, tn;
+        rs_tile(p, ps.cid + i * ps.nc, tm, tn);
+        const int m0 = tm * PAIR_M + static_cast<int>(crank ^ 1u) * BM;
+        if (m0 >= p.M) continue;  // a ragged last pair tile: the other CTA has no rows
+        const int j = m0 / p.Mb;
+        const int mt = (m0 - j * p.Mb) / 128;
+        const int n_first = (tn * BN) / 128;
+        for (int t = 0; t < BN / 128; ++t) {
+            const int ntile = n_first + t;
+            if (ntile >= p.T_fn) break;
+            const int slot = (j * p.T_fm + mt) * p.T_fn + ntile;
+            const uint64_t t0 = globaltimer();
+            for (uint32_t spin = 0;; ++spin) {
+                if (__all_sync(0xffffffffu, ld_acquire(p.flags + slot) >= e)) break;
+                __nanosleep(128);
+                if ((spin & 7u) == 7u) {
+                    if (aborted(ec)) return;
+                    if (globaltimer() - t0 > ec.timeout_ns) {
+                        if (lane == 0) raise_error(ec, OPW_ERR_TIMEOUT, j, slot);
+                        return;
+                    }
+                }
+            }
+            if (p.trace != nullptr && lane == 0) p.trace[F + slot] = globaltimer();
+            // 128 rows of up to 128 columns, 16 bytes per lane and step
+            const int col0 = ntile * 128;
+            const int vecs = (p.N - col0 < 128 ? p.N - col0 : 128) / 8;
+            const uint16_t* src = p.out_rank[j] + static_cast<int64_t>(m0 - j * p.Mb) * p.N + col0;
+            uint16_t* dst = p.recv + static_cast<int64_t>(m0) * p.N + col0;
+            for (int v = static_cast<int>(lane); v < 128 * vecs; v += 32) {
+                const int row = v / vecs;
+                const int c = (v - row * vecs) * 8;
+                const uint4 x = *reinterpret_cast<const uint4*>(src + static_cast<int64_t>(row) * p.N + c);
+                *reinterpret_cast<uint4*>(dst + static_cast<int64_t>(row) * p.N + c) = x;
+            }
+        }
+    }
 }
 
 __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_constant__ RsParams p)
@@ -357,6 +432,8 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
             rs_loader(p, smem, ctrl, ec, crank);
         } else if (warp == 1) {
             if (crank == 0) rs_mma(p, smem, ctrl, tmem, ec);
+        } else if (warp == 3) {
+            rs_receive(p, ec, crank);
         } else if (warp >= 4) {
             rs_reduce(p, smem, ctrl, tmem, ec, warp, crank);
         }

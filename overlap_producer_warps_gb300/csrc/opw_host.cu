@@ -223,6 +223,21 @@ opw_status ag_fill_params(const opw_symm* symm, size_t a_off, int64_t M_r, int64
     p.schedule = o.schedule;
     // Row groups only pay when B (K x N bf16) is too big to stay in L2.
     p.group_rows = (K * N * 2 > (int64_t(64) << 20)) ? 8 : 1;
+    // Ranks in the order the consumers take their rows: the local rank's own
+    // first, then the others in publish order (ring order after the local
+    // rank unless a publish order is given).  Rows are renamed rank by rank
+    // only when a rank's rows fill whole pair rows.
+    p.tpr = static_cast<int32_t>((M_r % PAIR_M == 0) ? M_r / PAIR_M : 0);
+    {
+        const int own = o.local_rank;
+        int k = 0;
+        if (own >= 0) p.visit[k++] = own;
+        for (int i = 0; i < R; ++i) {
+            const int r = o.publish_perm != nullptr ? o.publish_perm[i]
+                                                    : (own >= 0 ? (own + 1 + i) % R : i);
+            if (r != own && k < R) p.visit[k++] = r;
+        }
+    }
     p.signal_mode = o.signal_mode;
     p.has_perm = o.publish_perm != nullptr;
     p.has_delay = o.delay_ns != nullptr;
@@ -440,9 +455,15 @@ int64_t opw_rs_num_flags(int32_t R, int64_t M, int64_t N)
     return static_cast<int64_t>(R) * (M / R / 128) * ((N + 127) / 128);
 }
 
-opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t out_off, int64_t M,
-                       int64_t N, int64_t K_r, opw_signal* sig, uint64_t epoch,
-                       const opw_opts* opts_in, void* stream)
+}  // extern "C"
+
+namespace {
+
+// GEMM-RS launch shared by opw_gemm_rs and opw_gemm_rs_consume (recv_dev
+// NULL for the former).
+opw_status gemm_rs_launch(const opw_symm* symm, size_t a_off, size_t b_off, size_t out_off,
+                          int64_t M, int64_t N, int64_t K_r, void* recv_dev, opw_signal* sig,
+                          uint64_t epoch, const opw_opts* opts_in, void* stream)
 {
     opw_status st = check_symm(symm);
     if (st != OPW_OK) return st;
@@ -451,9 +472,11 @@ opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t 
     const opw_opts& o = opts_or_default(opts_in, tmp);
     if ((o.sync_mode != OPW_SYNC_OVERLAP && o.sync_mode != OPW_SYNC_CHECKED) || o.schedule != 0 ||
         o.role < OPW_ROLE_FUSED || o.role > OPW_ROLE_CONSUMER || o.publish_perm != nullptr ||
-        o.delay_ns != nullptr || o.fault_kind != 0 ||
+        o.delay_ns != nullptr || (o.fault_kind != OPW_FAULT_NONE && o.fault_kind != OPW_FAULT_DROP_TILE) ||
         o.num_ctas < 0 || o.signal_mode != 0 || o.local_rank < -1 || o.local_rank > 0)
         return OPW_ERR_INVALID_ARG;
+    // the receiving side waits on published tiles: only a fused launch publishes results
+    if (recv_dev != nullptr && o.role != OPW_ROLE_FUSED) return OPW_ERR_INVALID_ARG;
     const int R = symm->R;
     if (M <= 0 || N <= 0 || K_r <= 0 || M % (128 * R) != 0 || N % 8 != 0 || K_r % 8 != 0)
         return OPW_ERR_UNSUPPORTED_SHAPE;
@@ -461,6 +484,7 @@ opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t 
         return OPW_ERR_UNSUPPORTED_SHAPE;
     if (!aligned16(static_cast<int64_t>(a_off)) || !aligned16(static_cast<int64_t>(b_off)) ||
         !aligned16(static_cast<int64_t>(out_off)) ||
+        (recv_dev != nullptr && !aligned16(recv_dev)) ||
         (o.trace_dev != nullptr && (reinterpret_cast<uintptr_t>(o.trace_dev) & 7u) != 0))
         return OPW_ERR_MISALIGNED;
     const int64_t F = opw_rs_num_flags(R, M, N);
@@ -489,7 +513,9 @@ opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t 
             !make_map(&p.b_load[r], base + b_off, N, K_r, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !make_map(&p.out_store[r], base + out_off, N, Mb, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
             return OPW_ERR_CUDA;
+        p.out_rank[r] = reinterpret_cast<const uint16_t*>(base + out_off);
     }
+    p.recv = static_cast<uint16_t*>(recv_dev);
     p.flags = sig->flags;
     p.status = sig->status;
     p.trace = o.trace_dev;
@@ -502,15 +528,43 @@ opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t 
     p.Mb = static_cast<int32_t>(Mb);
     p.T_M = static_cast<int32_t>((M + 2 * BM - 1) / (2 * BM));
     p.T_N = static_cast<int32_t>((N + BN - 1) / BN);
+    // Groups of 8 pair rows: the pairs running at the same time (76 on a
+    // GB300) cover about 8 x 9 tiles instead of 5 x 16, reading fewer B_r
+    // column tiles per wave (measured on the tensor-parallel layer: 4 % fewer
+    // DRAM reads, 2.4 % faster than row order; groups of 16 read more).
+    p.group_rows = 8;
     p.T_fm = static_cast<int32_t>(Mb / 128);
     p.T_fn = static_cast<int32_t>((N + 127) / 128);
     p.checked = o.sync_mode == OPW_SYNC_CHECKED;
     p.role = o.role;
+    p.fault_kind = o.fault_kind;
+    p.fault_arg = o.fault_arg;
     if (launch_gemm_rs(p, pairs, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return OPW_ERR_CUDA;
     // The GEMM leg alone publishes nothing: the epoch stays the next one.
     if (o.role != OPW_ROLE_PRODUCER) sig->epoch_last = epoch;
     return OPW_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+opw_status opw_gemm_rs(const opw_symm* symm, size_t a_off, size_t b_off, size_t out_off, int64_t M,
+                       int64_t N, int64_t K_r, opw_signal* sig, uint64_t epoch,
+                       const opw_opts* opts_in, void* stream)
+{
+    return gemm_rs_launch(symm, a_off, b_off, out_off, M, N, K_r, nullptr, sig, epoch, opts_in,
+                          stream);
+}
+
+opw_status opw_gemm_rs_consume(const opw_symm* symm, size_t a_off, size_t b_off, size_t out_off,
+                               int64_t M, int64_t N, int64_t K_r, void* recv_dev, opw_signal* sig,
+                               uint64_t epoch, const opw_opts* opts_in, void* stream)
+{
+    if (recv_dev == nullptr) return OPW_ERR_INVALID_ARG;
+    return gemm_rs_launch(symm, a_off, b_off, out_off, M, N, K_r, recv_dev, sig, epoch, opts_in,
+                          stream);
 }
 
 }  // extern "C"

@@ -47,6 +47,9 @@ enum WaitSite : int32_t {
     SITE_SERIAL = 1009,
 };
 
+// Trace words of GEMM-RS: [0, F) publish time of each output flag slot,
+// [F, 2F) the time the receiving side acquired it.
+
 struct AgParams {
     CUtensorMap shard[OPW_MAX_RANKS];  // A_r [M_r, K], box {ft, 32}, no swizzle (producer load)
     CUtensorMap g_store;               // G [M, K], box {ft, 32}, no swizzle (producer store)
@@ -67,7 +70,10 @@ struct AgParams {
     int32_t T_mr, T_k;        // flag tiles per rank along M, along K
     int32_t T_M, T_N;         // PAIR_M x BN pair tiles along M, along N
     int32_t role, sync_mode, schedule;
-    int32_t group_rows;       // dynamic schedule: row tiles per rasterisation group
+    int32_t group_rows;       // both schedules: pair rows per rasterisation group
+    int32_t tpr;              // pair rows per rank (M_r / 256), 0 when a rank's rows are
+                              // not whole pair rows (then rows are taken in order)
+    int32_t visit[OPW_MAX_RANKS];  // ranks in the order the consumer takes their rows
     int32_t signal_mode;      // OPW_SIGNAL_TILE_SET or OPW_SIGNAL_ROW_ADD
     int32_t local_rank;       // the consumer's own rank (read in place, no flag wait), or -1
     int32_t has_perm, has_delay;
@@ -89,9 +95,15 @@ struct RsParams {
     uint64_t timeout_ns;
     int32_t R, M, N, K_r, Mb;
     int32_t T_M, T_N;         // 256 x 256 pair tiles along M, along N
+    int32_t group_rows;       // pair rows per rasterisation group of the tile order
     int32_t T_fm, T_fn;       // 128x128 flag tiles per rank block along M, along N
     int32_t checked;          // OPW_SYNC_CHECKED: publish by exchange, expect epoch-1
     int32_t role;             // OPW_ROLE_*: FUSED, PRODUCER (GEMM leg), CONSUMER (scatter leg)
+    int32_t fault_kind, fault_arg;  // OPW_FAULT_DROP_TILE: never publish flag slot fault_arg
+    // Receiving side (NULL recv: none): warp 3 of each CTA acquires the flags
+    // of the other CTA's output tiles and copies each into recv [M, N].
+    const uint16_t* out_rank[OPW_MAX_RANKS];  // out_j, [M/R, N] bf16
+    uint16_t* recv;
 };
 
 struct RingParams {

@@ -93,6 +93,10 @@ int main(void)
     /* calls that need a signal object refuse a null one */
     EXPECT(opw_ag_gemm(&symm, 0, 128, 256, 256, B, G, C, NULL, 1, NULL, NULL) == OPW_ERR_INVALID_ARG);
     EXPECT(opw_gemm_rs(&symm, 0, 0, 0, 256, 256, 128, NULL, 1, NULL, NULL) == OPW_ERR_INVALID_ARG);
+    EXPECT(opw_gemm_rs_consume(&symm, 0, 0, 0, 256, 256, 128, C, NULL, 1, NULL, NULL) ==
+           OPW_ERR_INVALID_ARG);
+    EXPECT(opw_gemm_rs_consume(&symm, 0, 0, 0, 256, 256, 128, NULL, NULL, 1, NULL, NULL) ==
+           OPW_ERR_INVALID_ARG);
     EXPECT(opw_signal_alloc(NULL, 16, NULL) == OPW_ERR_INVALID_ARG);
     EXPECT(opw_signal_free(NULL) == OPW_OK);
 

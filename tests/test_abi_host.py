@@ -189,7 +189,25 @@ def test_gemm_rs_rejects_bad_arguments_on_the_host(api):
     assert rs(opts=api.make_opts(role=3)) == E.ERR_INVALID_ARG
     assert rs(opts=api.make_opts(role=-1)) == E.ERR_INVALID_ARG
     assert rs(opts=api.make_opts(sync_mode=api.SYNC_SERIAL)) == E.ERR_INVALID_ARG
+    assert rs(opts=api.make_opts(fault_kind=api.FAULT_STALE_EPOCH)) == E.ERR_INVALID_ARG
     assert rs() == E.ERR_INVALID_ARG                    # too few slots
+
+
+def test_gemm_rs_consume_rejects_bad_arguments_on_the_host(api):
+    s = _fake_sig()
+    ns = _NoStream()
+
+    def rsc(recv=_Fake(0x900000), opts=None, M=512, N=256, K_r=128, R=2):
+        return api.gemm_rs_consume_status(_Fake(0x100000), [i * 65536 for i in range(R)], 0, 0,
+                                          0, M, N, K_r, recv, s, 1, opts, stream=ns)
+
+    assert rsc(recv=None) == api.ERR_INVALID_ARG
+    assert rsc(recv=_Fake(0x900008)) == api.ERR_MISALIGNED
+    # only a fused launch publishes results for the receiving side to wait on
+    assert rsc(opts=api.make_opts(role=api.ROLE_PRODUCER)) == api.ERR_INVALID_ARG
+    assert rsc(opts=api.make_opts(role=api.ROLE_CONSUMER)) == api.ERR_INVALID_ARG
+    assert rsc(N=12) == api.ERR_UNSUPPORTED_SHAPE
+    assert rsc() == api.ERR_INVALID_ARG                 # too few slots
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")

@@ -208,7 +208,8 @@ def _trace_views(api, prob, trace, grid):
                 F=F, T=T)
 
 
-def test_trace_publish_before_consume_and_swizzle_order(api):
+@pytest.mark.parametrize("local,perm", [(2, None), (0, None), (1, (3, 0, 2, 1))])
+def test_trace_publish_before_consume_and_swizzle_order(api, local, perm):
     R, M_r, K, N = 4, 256, 512, 1024
     d = inputs.ag_inputs(_cfg(R, M_r, K, N), seed=14)
     prob = AgProblem(d)
@@ -216,27 +217,37 @@ def test_trace_publish_before_consume_and_swizzle_order(api):
     words = api.ag_trace_words(R, M_r, N, K)
     trace = torch.full((words,), -1, dtype=torch.int64, device="cuda")
     grid = 6
-    prob.run(api, sig, sig.next_epoch(), api.make_opts(trace=trace, num_ctas=grid,
+    prob.run(api, sig, sig.next_epoch(), api.make_opts(trace=trace, num_ctas=grid, local_rank=local,
+                                                       publish_perm=perm,
                                                        schedule=api.SCHED_SWIZZLE))
     assert sig.status()[0] == api.OK
     v = _trace_views(api, prob, trace, grid)
     # every tile published; every tile of another rank acquired no earlier than
-    # its publish; the local rank's own tiles (rank 0 by default) never acquired
+    # its publish; the local rank's own tiles (read in place) never acquired
     per_rank = v["F"] // R
-    remote = np.arange(v["F"]) >= per_rank
+    remote = (np.arange(v["F"]) // per_rank) != local
     assert np.all(v["publish"] > 0)
     assert np.all(v["consume"][remote] != np.uint64(2 ** 64 - 1))
     assert np.all(v["publish"][remote] <= v["consume"][remote])
     assert np.all(v["consume"][~remote] == np.uint64(2 ** 64 - 1))
     # each consumer (a CTA pair) visited its 256x256 tiles in the oracle's
-    # swizzled order
+    # order: the page's rotation by the PE's rank (tiles_per_pe = M_r/256 = 1),
+    # or, with a publish order, the own rank first and then the others in it
     T_M, T_N, pairs = prob.M // 256, (N + 255) // 256, grid // 2
+    visit = None if perm is None else [local] + [r for r in perm if r != local]
     pair = (v["tile"] >> np.uint64(32)).astype(np.int64)
     pos = (v["tile"] & np.uint64(0xFFFFFFFF)).astype(np.int64)
     for c in range(pairs):
         mine = np.nonzero(pair == c)[0]
         got = mine[np.argsort(pos[mine])]
-        assert list(got) == list(oracle.consumer_order(T_M, T_N, R, pairs, c)), c
+        want = oracle.consumer_order(T_M, T_N, pairs, c, 1, local, M_r // 256, visit)
+        assert list(got) == list(want), c
+    if perm is not None:   # ranks published in the given order
+        pub = v["publish"].reshape(R, per_rank)
+        for i in range(1, R):
+            assert pub[perm[i - 1]].max() <= pub[perm[i]].min()
+    # the PE's first tile is on its own rows
+    assert oracle.consumer_order(T_M, T_N, pairs, 0, 1, local, 1)[0] == local * T_N
     G_ref, C_ref = prob.oracle_full()
     assert_gemm_close(host_bits(prob.C), C_ref)
 

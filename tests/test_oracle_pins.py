@@ -289,29 +289,34 @@ def test_swizzle_golden(golden):
         assert got == row, rank
     for case in fx["consumer_orders"]:
         for c, want in enumerate(case["orders"]):
-            got = oracle.consumer_order(case["T_M"], case["T_N"], case["R"], case["G"], c)
+            got = oracle.consumer_order(case["T_M"], case["T_N"], case["G"], c,
+                                        case["group_rows"], case["rank"], case["tiles_per_pe"],
+                                        case.get("visit"))
             assert list(got) == want, (case["note"], c)
 
 
-@pytest.mark.parametrize("T_M,T_N,R,G", [(64, 16, 8, 148), (64, 16, 8, 152), (16, 3, 4, 7),
-                                         (8, 1, 8, 3), (256, 32, 8, 152)])
-def test_consumer_order_is_a_partition_starting_at_home_rank(T_M, T_N, R, G):
-    seen = []
-    per = T_M // R
-    for c in range(G):
-        order = oracle.consumer_order(T_M, T_N, R, G, c)
-        seen.extend(order.tolist())
-        if len(order) == 0:
-            continue
-        assert all(q % G == c for q in order)
-        h = c % R
-        home = [q for q in order if (q // T_N) // per == h]
-        if home:   # starts on its own rank's rows when it owns any
-            assert order[0] == min(home)
-        # visiting order is the swizzled row order
-        keys = [(((q // T_N) - h * per) % T_M, q % T_N) for q in order]
-        assert keys == sorted(keys)
-    assert sorted(seen) == list(range(T_M * T_N))
+@pytest.mark.parametrize("T_M,T_N,G,GM,rank,tpp", [(32, 16, 76, 1, 0, 4), (64, 14, 76, 1, 3, 8),
+                                                   (128, 32, 76, 8, 5, 16), (9, 3, 4, 8, 1, 1),
+                                                   (16, 3, 7, 2, 3, 4), (8, 1, 3, 1, 7, 1)])
+def test_consumer_order_is_a_partition_starting_at_own_rows(T_M, T_N, G, GM, rank, tpp):
+    orders = [oracle.consumer_order(T_M, T_N, G, c, GM, rank, tpp) for c in range(G)]
+    seen = np.concatenate(orders)
+    assert sorted(seen.tolist()) == list(range(T_M * T_N))           # every tile exactly once
+    assert max(len(o) for o in orders) == -(-T_M * T_N // G)          # balanced
+    # consumer 0 starts on the PE's own first row, column 0
+    assert orders[0][0] == ((rank * tpp) % T_M) * T_N
+    # undoing the rename gives rows that never go backwards, group by group
+    for o in orders:
+        rows = [((q // T_N) - rank * tpp) % T_M for q in o]
+        assert [r // GM for r in rows] == sorted(r // GM for r in rows)
+    # the rank visit order of a ring (own rank, then rank+1, rank+2, ...) is
+    # the page's formula, whenever the row tiles split evenly over the ranks
+    if T_M % tpp == 0:
+        R = T_M // tpp
+        ring = [(rank + k) % R for k in range(R)]
+        for c in range(G):
+            assert list(oracle.consumer_order(T_M, T_N, G, c, GM, rank, tpp, ring)) == \
+                list(orders[c])
 
 
 # ---------------------------------------------------------------- ring AllReduce

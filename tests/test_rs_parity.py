@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from overlap_producer_warps_gb300 import inputs
-from tests.helpers import RsProblem, assert_gemm_close, sample_rows
+from tests.helpers import RsProblem, assert_gemm_close, quarter_rows, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -193,3 +193,110 @@ def test_full_size_tp_sampled(api):
     assert np.all(sig.flags().cpu().numpy() == 2)
     rows = sample_rows(prob.M, 128, 1, seed=2)
     _check_all(api, prob, rows)
+
+
+# ---------------------------------------------------------------- receiving side
+
+def _out_regions(prob):
+    d, n = prob.d, prob.Mb * prob.N * 2
+    return [prob.heap[int(prob.rank_off[j]) + d["out_off"]:int(prob.rank_off[j]) + d["out_off"] + n]
+            for j in range(prob.R)]
+
+
+def _consume(api, prob, sig, epoch, opts=None):
+    """One GEMM-RS launch with the receiving side, into a NaN-filled recv
+    buffer, with every rank's output block first filled with NaN bits too (a
+    copy taken before a tile's store landed would show)."""
+    d = prob.d
+    for reg in _out_regions(prob):
+        reg.fill_(0xFF)
+    recv = torch.full((prob.M, prob.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    api.gemm_rs_consume(prob.heap, prob.rank_off, d["a_off"], d["b_off"], d["out_off"], prob.M,
+                        prob.N, prob.K_r, recv, sig, epoch, opts)
+    return recv
+
+
+@pytest.mark.parametrize("R,M,K_r,N,num_ctas", [
+    (3, 1152, 192, 328, 0),   # ragged last pair tile (the odd CTA has no rows) and ragged N
+    (4, 1024, 448, 1024, 2),  # one pair: its odd CTA receives every tile the even one stores
+    (2, 256, 128, 200, 0),
+])
+def test_receiving_side_acquires_every_tile_before_copying(api, R, M, K_r, N, num_ctas):
+    d = inputs.rs_inputs(_cfg(R, M, K_r, N), seed=80 + R)
+    prob = RsProblem(d)
+    F = api.rs_num_flags(R, M, N)
+    sig = api.Signal(F)
+    trace = torch.full((2 * F,), -1, dtype=torch.int64, device="cuda")
+    for _ in range(2):
+        trace.fill_(-1)
+        e = sig.next_epoch()
+        recv = _consume(api, prob, sig, e, api.make_opts(trace=trace, num_ctas=num_ctas))
+        st = sig.status()
+        assert st[0] == api.OK, st
+        assert np.array_equal(sig.flags().cpu().numpy(), oracle.expected_flags(F, e))
+        # the receiver's copy is every rank's block, bit for bit
+        got = recv.view(torch.int16).cpu().numpy().view(np.uint16)
+        want = np.concatenate([prob.out_bits(j) for j in range(R)])
+        assert np.array_equal(got, want)
+        # every tile published, every tile acquired, never before its publish
+        t = trace.cpu().numpy().view(np.uint64)
+        pub, got_at = t[:F], t[F:2 * F]
+        none = np.uint64(2 ** 64 - 1)
+        assert np.all(pub != none) and np.all(got_at != none)
+        assert np.all(pub <= got_at)
+    _check_all(api, prob)
+
+
+def test_receiving_side_with_checked_publish(api):
+    R, M, K_r, N = 4, 1024, 256, 512
+    d = inputs.rs_inputs(_cfg(R, M, K_r, N), seed=85)
+    prob = RsProblem(d)
+    F = api.rs_num_flags(R, M, N)
+    sig = api.Signal(F)
+    for _ in range(3):
+        e = sig.next_epoch()
+        recv = _consume(api, prob, sig, e, api.make_opts(sync_mode=api.SYNC_CHECKED))
+        assert sig.status()[0] == api.OK
+        got = recv.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, np.concatenate([prob.out_bits(j) for j in range(R)]))
+    _check_all(api, prob)
+
+
+def test_receiving_side_times_out_on_a_missing_flag_and_recovers(api):
+    """A tile whose flag is never published: the receiving wait runs out and
+    latches TIMEOUT with that tile's rank and slot; after a reset the next
+    launch is correct."""
+    R, M, K_r, N = 2, 512, 128, 512
+    d = inputs.rs_inputs(_cfg(R, M, K_r, N), seed=86)
+    prob = RsProblem(d)
+    F = api.rs_num_flags(R, M, N)
+    sig = api.Signal(F)
+    slot = 9
+    _consume(api, prob, sig, sig.next_epoch(),
+             api.make_opts(timeout_ns=50_000_000, fault_kind=api.FAULT_DROP_TILE, fault_arg=slot))
+    status, rank, where = sig.status()
+    assert status == api.ERR_TIMEOUT
+    assert (rank, where) == (slot // (F // R), slot)
+    sig.reset()
+    recv = _consume(api, prob, sig, sig.next_epoch())
+    assert sig.status()[0] == api.OK
+    got = recv.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, np.concatenate([prob.out_bits(j) for j in range(R)]))
+    _check_all(api, prob)
+
+
+def test_full_size_tp_with_receiving_side(api):
+    """GEMM-RS TP at full size with the receiving side: recv bit-equal to the
+    blocks, the blocks within the tolerance on sampled rows."""
+    cfg = inputs.CONFIGS["rs_tp"]
+    prob = RsProblem(inputs.rs_inputs(cfg, seed=0))
+    F = api.rs_num_flags(prob.R, prob.M, prob.N)
+    sig = api.Signal(F)
+    trace = torch.full((2 * F,), -1, dtype=torch.int64, device="cuda")
+    recv = _consume(api, prob, sig, sig.next_epoch(), api.make_opts(trace=trace))
+    assert sig.status()[0] == api.OK
+    got = recv.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, np.concatenate([prob.out_bits(j) for j in range(prob.R)]))
+    t = trace.cpu().numpy().view(np.uint64)
+    assert np.all(t[:F] <= t[F:2 * F])
+    _check_all(api, prob, quarter_rows(prob.M, seed=4))
