@@ -134,22 +134,35 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sel)}
 
 
+TRAFFIC_SOURCES = ("opw_device.cuh", "opw_kernels.h", "opw_host.cu")
+
+
+def source_hashes(kernel_source: str) -> dict:
+    """sha256[:16] of the kernel's source and of the shared sources that shape
+    its launch (device helpers, parameter blocks, host-side tile order)."""
+    out = {}
+    for f in (kernel_source,) + TRAFFIC_SOURCES:
+        path = os.path.join(ROOT, "overlap_producer_warps_gb300", "csrc", f)
+        out[f] = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    return out
+
+
 def kernel_traffic(name: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+    the current sources (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     ent = d.get(name)
-    if not ent:
+    if not ent or "sources" not in ent:
         return None
-    src = os.path.join(ROOT, "overlap_producer_warps_gb300", "csrc", ent["source"])
-    if not os.path.exists(src):
+    try:
+        now = source_hashes(ent["source"])
+    except OSError:
         return None
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return ent["dram_bytes_per_launch"] if h == ent.get("source_sha256_16") else None
+    return ent["dram_bytes_per_launch"] if now == ent["sources"] else None
 
 
 def reduce_max(x: float, dist, device) -> float:
@@ -375,7 +388,27 @@ def time_launches(torch, fn, n, warm=2):
         ev[i + 1].record(s)
     ev[n].synchronize()
     t = [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
-    return {"mean": statistics.mean(t), "median": statistics.median(t), "min": min(t), "n": n}
+    return {"mean": statistics.mean(t), "median": statistics.median(t), "min": min(t), "n": n,
+            "all": t}
+
+
+def time_interleaved(torch, fns, rounds=5, per_round=4):
+    """Device times of several variants measured in interleaved rounds (each
+    round runs every variant for per_round launches), so that no variant is
+    favoured by the clock state (boost versus the power cap) it happens to
+    run in.  Returns {name: {mean, median, min, n}} over all rounds."""
+    samples = {k: [] for k in fns}
+    for _ in range(rounds):
+        for k, fn in fns.items():
+            t = time_launches(torch, fn, per_round, warm=1)
+            samples[k].extend(t["all"])
+    return {k: {"mean": statistics.mean(v), "median": statistics.median(v), "min": min(v),
+                "n": len(v)} for k, v in samples.items()}
+
+
+def _summ(t):
+    """A time_launches() result without the per-launch list."""
+    return {k: v for k, v in t.items() if k != "all"}
 
 
 def tflops_of(flops, t):
@@ -407,7 +440,7 @@ def ring_results(api, torch, reps, R=8, n=8 * (1 << 21)):
     gbs = algo_bytes / (t["median"] * 1e-3) / 1e9
     busbw = 2 * (R - 1) / R * n * 4 / (t["median"] * 1e-3) / 1e9
     sig.close()
-    return {"ranks": R, "values_per_rank": n, "ms": t, "hbm_gbs": gbs,
+    return {"ranks": R, "values_per_rank": n, "ms": _summ(t), "hbm_gbs": gbs,
             "hbm_frac": gbs / float(peaks["hbm_gbs"]), "algo_bytes": algo_bytes,
             "busbw_gbs": busbw}
 
@@ -430,7 +463,7 @@ def alltoall_results(api, torch, reps, R=8, B=8 << 20):
     moved = 2 * R * R * B  # every slice read once and written once
     gbs = moved / (t["median"] * 1e-3) / 1e9
     sig.close()
-    return {"ranks": R, "bytes_per_slice": B, "ms": t, "hbm_gbs": gbs,
+    return {"ranks": R, "bytes_per_slice": B, "ms": _summ(t), "hbm_gbs": gbs,
             "hbm_frac": gbs / float(peaks["hbm_gbs"])}
 
 
@@ -444,8 +477,8 @@ def ag_fused_results(api, torch, name, reps, producer_only=False):
     d = w.d
     w.close()
     if producer_only:
-        return {"ms": t, "gather_hbm_gbs": 2.0 * w.M * d["K"] * 2 / (t["median"] * 1e-3) / 1e9}
-    return {"ms": t, **tflops_of(w.flops, t)}
+        return {"ms": _summ(t), "gather_hbm_gbs": 2.0 * w.M * d["K"] * 2 / (t["median"] * 1e-3) / 1e9}
+    return {"ms": _summ(t), **tflops_of(w.flops, t)}
 
 
 def rs_results(api, torch, reps, scatter_only=False):
@@ -466,8 +499,8 @@ def rs_results(api, torch, reps, scatter_only=False):
         raise RuntimeError(f"rs_tp: device error {st}")
     sig.close()
     if scatter_only:
-        return {"ms": t, "scatter_hbm_gbs": M * N * 2 / (t["median"] * 1e-3) / 1e9}
-    return {"ms": t, **tflops_of(flops_rs(cfg), t)}
+        return {"ms": _summ(t), "scatter_hbm_gbs": M * N * 2 / (t["median"] * 1e-3) / 1e9}
+    return {"ms": _summ(t), **tflops_of(flops_rs(cfg), t)}
 
 
 def tiny_results(api, torch, reps=50):
@@ -509,16 +542,11 @@ def mm_f32_out(torch):
 def ag_config_results(api, torch, name, peak_tflops, reps):
     """One AG-GEMM layer: fused (default schedule), the page's static swizzle,
     serial sync, batched row signals, the legs alone, unfused copy-then-GEMM
-    and cuBLAS on the pre-gathered G, each over `reps` launches."""
+    and cuBLAS on the pre-gathered G, measured in interleaved rounds."""
     w = AgLayer(api, torch, name)
     d, cfg = w.d, w.cfg
     R, M_r, K, N = d["R"], d["M_r"], d["K"], d["N"]
     x = w.bufs[0]
-    t = {}
-    t["fused"] = time_launches(torch, w.launch, reps)
-    t["swizzle"] = time_launches(torch, lambda: w.launch(schedule=api.SCHED_SWIZZLE), reps)
-    # every consumer waits for the whole gather before its first tile
-    t["serial"] = time_launches(torch, lambda: w.launch(sync_mode=api.SYNC_SERIAL), reps)
     sig_add = api.Signal(api.ag_num_row_counters(R, M_r, K))
 
     def fused_row_add():
@@ -526,21 +554,6 @@ def ag_config_results(api, torch, name, peak_tflops, reps):
                     sig_add, sig_add.next_epoch(),
                     skew_opts(api, cfg, signal_mode=api.SIGNAL_ROW_ADD))
 
-    t["row_add"] = time_launches(torch, fused_row_add, reps)
-    if sig_add.status()[0] != api.OK:
-        raise RuntimeError(f"{name}: device error with row-ADD signals")
-    sig_add.close()
-    if cfg.get("skew"):
-        # the publish order without the per-rank delays
-        from overlap_producer_warps_gb300 import inputs
-        perm, _ = inputs.skew_schedule(0, R)
-        t["no_delay"] = time_launches(torch, lambda: api.ag_gemm(
-            x["heap"], d["rank_off"], d["a_off"], M_r, N, K, x["B"], x["G"], x["C"], w.sig,
-            w.sig.next_epoch(), api.make_opts(publish_perm=perm)), reps)
-    t["producer_only"] = time_launches(torch, lambda: w.launch(role=api.ROLE_PRODUCER), reps)
-    t["consumer_only"] = time_launches(
-        torch, lambda: w.launch(epoch=w.sig.next_epoch() - 1, role=api.ROLE_CONSUMER), reps)
-    w.check()
     shards = [x["heap"][int(d["rank_off"][r]):int(d["rank_off"][r]) + M_r * K * 2]
               .view(torch.bfloat16).view(M_r, K) for r in range(R)]
     G, B, C = x["G"], x["B"], x["C"]
@@ -550,8 +563,30 @@ def ag_config_results(api, torch, name, peak_tflops, reps):
             G[r * M_r:(r + 1) * M_r].copy_(shards[r])
         torch.matmul(G, B, out=C)
 
-    t["unfused"] = time_launches(torch, unfused, reps)
-    t["gemm_only"] = time_launches(torch, lambda: torch.matmul(G, B, out=C), reps)
+    fns = {"fused": w.launch,
+           "swizzle": lambda: w.launch(schedule=api.SCHED_SWIZZLE),
+           # every consumer waits for the whole gather before its first tile
+           "serial": lambda: w.launch(sync_mode=api.SYNC_SERIAL),
+           "row_add": fused_row_add,
+           "producer_only": lambda: w.launch(role=api.ROLE_PRODUCER),
+           # flags still hold the epoch the previous launch published
+           "consumer_only": lambda: w.launch(epoch=w.sig.next_epoch() - 1,
+                                             role=api.ROLE_CONSUMER),
+           "unfused": unfused,
+           "gemm_only": lambda: torch.matmul(G, B, out=C)}
+    if cfg.get("skew"):
+        # the publish order without the per-rank delays
+        from overlap_producer_warps_gb300 import inputs
+        perm, _ = inputs.skew_schedule(0, R)
+        no_delay = api.make_opts(publish_perm=perm)
+        fns["no_delay"] = lambda: api.ag_gemm(
+            x["heap"], d["rank_off"], d["a_off"], M_r, N, K, x["B"], x["G"], x["C"], w.sig,
+            w.sig.next_epoch(), no_delay)
+    t = time_interleaved(torch, fns, rounds=max(1, reps // 4), per_round=4)
+    w.check()
+    if sig_add.status()[0] != api.OK:
+        raise RuntimeError(f"{name}: device error with row-ADD signals")
+    sig_add.close()
     fl = w.flops
     med = {k: v["median"] for k, v in t.items()}
     e = (med["producer_only"] + med["consumer_only"] - med["fused"]) / min(
@@ -581,7 +616,7 @@ def ag_config_results(api, torch, name, peak_tflops, reps):
 def rs_config_results(api, torch, peak_tflops, reps):
     """GEMM-RS TP: fused, the legs alone, the unfused path (fp32 partials, an
     fp32 sum in rank order, then the row blocks split off) and one cuBLAS GEMM
-    with the same FLOPs."""
+    with the same FLOPs, measured in interleaved rounds."""
     from overlap_producer_warps_gb300 import inputs
     cfg = inputs.CONFIGS["rs_tp"]
     d = inputs.rs_inputs(cfg, seed=0)
@@ -593,10 +628,6 @@ def rs_config_results(api, torch, peak_tflops, reps):
         api.gemm_rs(heap, d["rank_off"], d["a_off"], d["b_off"], d["out_off"], M, N, K_r, sig,
                     sig.next_epoch(), api.make_opts(role=role))
 
-    t = {}
-    t["fused"] = time_launches(torch, rs, reps)
-    t["gemm_leg_only"] = time_launches(torch, lambda: rs(api.ROLE_PRODUCER), reps)
-    t["scatter_leg_only"] = time_launches(torch, lambda: rs(api.ROLE_CONSUMER), reps)
     A = [heap[int(d["rank_off"][r]) + d["a_off"]:int(d["rank_off"][r]) + d["a_off"] + M * K_r * 2]
          .view(torch.bfloat16).view(M, K_r) for r in range(R)]
     Bs = [heap[int(d["rank_off"][r]) + d["b_off"]:int(d["rank_off"][r]) + d["b_off"] + K_r * N * 2]
@@ -612,13 +643,16 @@ def rs_config_results(api, torch, peak_tflops, reps):
         for j in range(R):
             outs[j].copy_(S[j * (M // R):(j + 1) * (M // R)])
 
-    t["unfused"] = time_launches(torch, unfused_rs, reps)
     # The same FLOPs as one cuBLAS GEMM with the ranks' K slices side by side
     # ([M, R*K_r] @ [R*K_r, N]): no per-rank partials, no reduction, no scatter.
     A_cat = torch.cat(A, dim=1)
     B_cat = torch.cat(Bs, dim=0)
     C_cat = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    t["gemm_only"] = time_launches(torch, lambda: torch.matmul(A_cat, B_cat, out=C_cat), reps)
+    t = time_interleaved(torch, {
+        "fused": rs, "gemm_leg_only": lambda: rs(api.ROLE_PRODUCER),
+        "scatter_leg_only": lambda: rs(api.ROLE_CONSUMER), "unfused": unfused_rs,
+        "gemm_only": lambda: torch.matmul(A_cat, B_cat, out=C_cat)},
+        rounds=max(1, reps // 4), per_round=4)
     del A_cat, B_cat, C_cat
     st = sig.status()
     if st[0] != api.OK:
@@ -648,7 +682,7 @@ def tp_layer_results(api, torch, peak_tflops, reps):
     w.close()
     return {"workload": TP_WORKLOAD, "step_tflops": fl / t["median"] / 1e9,
             "step_tflops_best": fl / t["min"] / 1e9,
-            "pct_of_peak": fl / t["median"] / 1e9 / peak_tflops, "ms": t}
+            "pct_of_peak": fl / t["median"] / 1e9 / peak_tflops, "ms": _summ(t)}
 
 
 def per_config_results(api, torch, peak_tflops, reps=20):
