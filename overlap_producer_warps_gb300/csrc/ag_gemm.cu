@@ -48,8 +48,13 @@
 namespace opw {
 namespace {
 
-constexpr int AG_STAGES = 5;
-constexpr int GATHER_BUFS = 4;  // producer staging buffers (a power of 2)
+// A 6-stage ring with 2 gather staging buffers fits the budget (225 KiB);
+// against 5 stages with 4 buffers it was 1.3-2.2 % faster fused on every
+// layer in a burst, about even under the power cap, and its gather alone
+// 15 % slower (hidden in the fused kernel).
+constexpr int AG_STAGES = 6;
+constexpr int GATHER_BUFS = 2;    // the fused kernel's producer staging buffers
+constexpr int PROD_BUFS = 4;      // per producer warp when the gather runs alone
 constexpr int HALF_N = BN / 2;                  // B columns held by each CTA
 constexpr int B_HALF_BYTES = BK * HALF_N * 2;   // 16 KiB: 2 chunks of 64 columns
 constexpr uint32_t PAIR_TX_BYTES = 2u * (A_STAGE_BYTES + B_HALF_BYTES);
@@ -60,6 +65,7 @@ struct AgCtrl {
     uint64_t tmem_full[2];      // each CTA: an accumulator is complete in its TMEM
     uint64_t tmem_empty[2];     // even CTA: both CTAs' epilogues have read it
     uint64_t gfull[GATHER_BUFS];
+    uint64_t gprod[8 * PROD_BUFS];  // producer-only role: PROD_BUFS per producer warp
     uint64_t tq_full[TILE_Q];   // each CTA: a tile id is in its queue slot
     uint64_t tq_empty[TILE_Q];  // even CTA: its readers of the slot and the odd CTA's forwarder are done
     uint64_t tq_fwd[TILE_Q];    // odd CTA: its readers of the slot are done
@@ -77,6 +83,12 @@ constexpr int OFF_GATHER = OFF_EPI + 4 * EPI_WARP_BYTES;
 constexpr int OFF_CTRL = OFF_GATHER + GATHER_BUFS * GATHER_BUF_BYTES;
 constexpr int SMEM_ALLOC = OFF_CTRL + static_cast<int>(sizeof(AgCtrl)) + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget (227 KiB per CTA)");
+// With the gather alone (OPW_ROLE_PRODUCER) the consumer warps are idle and
+// their shared memory is free: warp w < PROD_WARPS gathers through its own
+// PROD_BUFS staging buffers at OFF_A + w * PROD_BUFS * GATHER_BUF_BYTES.
+constexpr int PROD_WARPS_FIT = OFF_CTRL / (PROD_BUFS * GATHER_BUF_BYTES);
+constexpr int PROD_WARPS = PROD_WARPS_FIT < 8 ? PROD_WARPS_FIT : 8;
+static_assert(PROD_WARPS >= 1, "room for at least one producer warp");
 static_assert(OFF_B % 1024 == 0 && OFF_EPI % 1024 == 0 && OFF_GATHER % 1024 == 0,
               "swizzled buffers must be 1024-byte aligned");
 
@@ -665,14 +677,16 @@ __device__ __forceinline__ void publish_tile(const AgParams& p, const ErrCtx& ec
 // as it lands.  The next tile's loads are issued before the previous tile's
 // stores are waited for and its flag published, and the next claim is made
 // while the current tile is in flight.
-__device__ void run_gather(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const ErrCtx& ec,
-                           uint64_t t_start)
+// buf0 / gfull: this warp's nb staging buffers (GATHER_BUF_BYTES each) and
+// their barriers.
+__device__ void run_gather(const AgParams& p, uint8_t* buf0, uint64_t* gfull, int nb,
+                           const ErrCtx& ec, uint64_t t_start)
 {
     const uint32_t lane = lane_id();
     const int n_items = p.R * p.T_mr * p.T_k;
-    const int subs = p.ft / GATHER_SUB_ROWS;  // 2 or 4, at most GATHER_BUFS
+    const int subs = p.ft / GATHER_SUB_ROWS;  // 2 or 4
+    const uint32_t unb = static_cast<uint32_t>(nb);
     const uint32_t sub_bytes = static_cast<uint32_t>(p.ft) * GATHER_SUB_ROWS * 2u;
-    uint8_t* buf0 = smem + OFF_GATHER;
     unsigned long long* claim_ctr = p.counters + CTR_GATHER;
 
     auto claimed = [&](unsigned long long raw) -> int {
@@ -684,7 +698,7 @@ __device__ void run_gather(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
     int cur = claimed(raw);
 
     int ordered_upto = 0;  // rank positions whose predecessors are known complete
-    uint32_t seq = 0;      // sub-box sequence number: buffer seq % GATHER_BUFS
+    uint32_t seq = 0;      // sub-box sequence number: buffer seq % nb
     bool pending = false;  // `pend` is copied (stores committed) but not yet published
     GatherItem pend{0, 0, 0, 0};
     bool ok = true;
@@ -737,20 +751,23 @@ __device__ void run_gather(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
             ordered_upto = g.ip;
         }
 
-        // Loads of this tile.  Its buffers were last read by the previous
-        // tile's stores: those must have finished reading shared memory.
+        // Loads of this tile, as many as there are staging buffers.  The
+        // buffers were last read by the previous tile's stores: those must
+        // have finished reading shared memory.
         const int x = g.kt * p.ft;
         const int y_src = g.mt * p.ft;
         const int y_dst = g.r * p.M_r + g.mt * p.ft;
+        auto issue_load = [&](int sub) {  // lane 0
+            const uint32_t sq = seq + static_cast<uint32_t>(sub);
+            uint64_t* fb = &gfull[sq % unb];
+            mbar_arrive_expect_tx(fb, sub_bytes);
+            tma_load_2d(buf0 + (sq % unb) * GATHER_BUF_BYTES, &p.shard[g.r], fb, x,
+                        y_src + sub * GATHER_SUB_ROWS);
+        };
+        const int ahead = subs < nb ? subs : nb;
         if (lane == 0) {
             bulk_wait_read<0>();
-            for (int sub = 0; sub < subs; ++sub) {
-                const uint32_t sq = seq + static_cast<uint32_t>(sub);
-                uint64_t* fb = &ctrl->gfull[sq % GATHER_BUFS];
-                mbar_arrive_expect_tx(fb, sub_bytes);
-                tma_load_2d(buf0 + (sq % GATHER_BUFS) * GATHER_BUF_BYTES, &p.shard[g.r], fb, x,
-                            y_src + sub * GATHER_SUB_ROWS);
-            }
+            for (int sub = 0; sub < ahead; ++sub) issue_load(sub);
         }
         __syncwarp();
         // The previous tile's stores are the only ones committed: wait for
@@ -760,23 +777,28 @@ __device__ void run_gather(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
             __syncwarp();
             pending = false;
         }
-        // Store each sub-box into G as it lands.
+        // Store each sub-box into G as it lands; refill its buffer with a
+        // later sub-box of the tile once the store has read it.
         for (int sub = 0; sub < subs; ++sub) {
             const uint32_t sq = seq + static_cast<uint32_t>(sub);
-            if (!wait_bar(&ctrl->gfull[sq % GATHER_BUFS], (sq / GATHER_BUFS) & 1u, ec,
-                          SITE_GATHER_LOAD)) {
+            if (!wait_bar(&gfull[sq % unb], (sq / unb) & 1u, ec, SITE_GATHER_LOAD)) {
                 // every outstanding load must land before the CTA may exit
-                for (int k = sub; k < subs; ++k) {
+                const int issued = sub + nb < subs ? sub + nb : subs;
+                for (int k = sub; k < issued; ++k) {
                     const uint32_t sk = seq + static_cast<uint32_t>(k);
-                    drain_bar(&ctrl->gfull[sk % GATHER_BUFS], (sk / GATHER_BUFS) & 1u, ec);
+                    drain_bar(&gfull[sk % unb], (sk / unb) & 1u, ec);
                 }
                 ok = false;
                 break;
             }
             if (lane == 0) {
-                tma_store_2d(&p.g_store, buf0 + (sq % GATHER_BUFS) * GATHER_BUF_BYTES, x,
+                tma_store_2d(&p.g_store, buf0 + (sq % unb) * GATHER_BUF_BYTES, x,
                              y_dst + sub * GATHER_SUB_ROWS);
                 bulk_commit();
+                if (sub + nb < subs) {
+                    bulk_wait_read<0>();
+                    issue_load(sub + nb);
+                }
             }
             __syncwarp();
         }
@@ -813,6 +835,7 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
             mbar_init(&ctrl->tmem_empty[i], 2 * 4);  // 4 epilogue warps in each CTA
         }
         for (int i = 0; i < GATHER_BUFS; ++i) mbar_init(&ctrl->gfull[i], 1);
+        for (int i = 0; i < PROD_WARPS * PROD_BUFS; ++i) mbar_init(&ctrl->gprod[i], 1);
         for (int i = 0; i < TILE_Q; ++i) {
             mbar_init(&ctrl->tq_full[i], 1);
             mbar_init(&ctrl->tq_empty[i], TQ_READERS);
@@ -850,13 +873,19 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
     // The pair follows the even CTA's start-up decision, so both run or neither does.
     const bool skip = ld_shared_cluster_u32(mapa_shared(smem_u32(&ctrl->abort), 0)) != 0;
 
-    if (!skip) {
+    if (!skip && !consumer) {
+        // the gather alone: every warp that has room in the idle shared memory
+        if (warp < PROD_WARPS)
+            run_gather(p, smem + OFF_A + warp * PROD_BUFS * GATHER_BUF_BYTES,
+                       &ctrl->gprod[warp * PROD_BUFS], PROD_BUFS, ec, t_start);
+    } else if (!skip) {
         if (warp == 0) {
             if (consumer) run_loader(p, smem, ctrl, ec, crank);
         } else if (warp == 1) {
             if (consumer && crank == 0) run_mma(p, smem, ctrl, tmem, ec);
         } else if (warp == 2) {
-            if (producer) run_gather(p, smem, ctrl, ec, t_start);
+            if (producer)
+                run_gather(p, smem + OFF_GATHER, ctrl->gfull, GATHER_BUFS, ec, t_start);
         } else if (warp == 3) {
             if (consumer && crank == 0) run_scheduler(p, ctrl, ec);
             if (consumer && crank == 1) run_forwarder(ctrl, ec);
@@ -910,6 +939,8 @@ bool set_smem_attr()
 }  // namespace
 
 size_t ag_smem_bytes() { return SMEM_ALLOC; }
+
+int ag_producer_warps(int role) { return role == OPW_ROLE_PRODUCER ? PROD_WARPS : 1; }
 
 int ag_max_pairs()
 {

@@ -438,9 +438,11 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
     sig->mode_tk = K / ft;
     if (produces) {
         sig->epoch_last = epoch;
-        // every flag tile is claimed once, and every CTA's producer makes one
+        // every flag tile is claimed once, and every producer warp makes one
         // claim past the end
-        sig->gather_next += per_rank * static_cast<uint64_t>(R) + 2u * static_cast<uint64_t>(pairs);
+        sig->gather_next += per_rank * static_cast<uint64_t>(R) +
+                            2u * static_cast<uint64_t>(pairs) *
+                                static_cast<uint64_t>(ag_producer_warps(o.role));
         for (int r = 0; r < R; ++r) {
             sig->rank_target_last[r] = p.rank_target[r];
             sig->rank_done[r] = p.rank_target[r];

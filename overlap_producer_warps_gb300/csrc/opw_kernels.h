@@ -125,6 +125,7 @@ size_t ag_smem_bytes();
 size_t rs_smem_bytes();
 
 int ag_max_pairs();  // clusters of 2 AG-GEMM CTAs that fit at once (0 on error)
+int ag_producer_warps(int role);  // gathering warps per CTA for OPW_ROLE_* role
 
 // AG-GEMM host set-up shared by the two entry points (opw_host.cu).
 // ag_check_args: every argument check that needs no CUDA call; *ft = flag tile.
