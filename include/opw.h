@@ -110,7 +110,10 @@ opw_status opw_signal_flags(const opw_signal* sig, int64_t** flags_dev, int64_t*
  * Synchronise `stream`, then read and return the device status word.  If a
  * device-side error was latched, *rank / *tile (either may be NULL) receive
  * the logical rank and flag slot the failing wait was on (-1 if none).
- * The latched error stays until opw_signal_reset().
+ * The latched error stays until opw_signal_reset().  Every device-side wait
+ * on a signal ("Distributed Architecture Design" 6.3, wait until the signal
+ * satisfies its predicate) is bounded by opts.timeout_ns; a wait that runs
+ * out is reported here instead of hanging.
  */
 opw_status opw_status_sync(opw_signal* sig, void* stream, int32_t* rank, int32_t* tile);
 
@@ -206,10 +209,12 @@ void opw_opts_default(opw_opts* o);
 /* ---------------------------------------------------------------- AG-GEMM */
 
 /*
- * Flag tile (square, in elements) used for shapes (M_r, K): 128 when both
- * are multiples of 128, else 64.  Flag slot of tile (r, mt, kt):
- * (r * (M_r/ft) + mt) * (K/ft) + kt.  Returns the slot count, or -1 for
- * invalid sizes.
+ * Sizing of the signal object for AG-GEMM ("Signal-Based Synchronization":
+ * one signal per tile; "AllGather and GEMM Overlapping" step 2, a signal
+ * after each tile transfer).  Flag tile (square, in elements) used for
+ * shapes (M_r, K): 128 when both are multiples of 128, else 64.  Flag slot
+ * of tile (r, mt, kt): (r * (M_r/ft) + mt) * (K/ft) + kt.  Returns the slot
+ * count, or -1 for invalid sizes.
  */
 int64_t opw_ag_flag_tile(int64_t M_r, int64_t K);
 int64_t opw_ag_num_flags(int32_t R, int64_t M_r, int64_t K);
@@ -219,7 +224,9 @@ int64_t opw_ag_num_flags(int32_t R, int64_t M_r, int64_t K);
 int64_t opw_ag_num_row_counters(int32_t R, int64_t M_r, int64_t K);
 
 /*
- * Trace layout (uint64 words), written only when opts.trace_dev != NULL:
+ * Trace of an AG-GEMM launch: the order checks of "Best Practices" 6
+ * (profile the overlap and the synchronization).  Layout (uint64 words),
+ * written only when opts.trace_dev != NULL:
  *   [0, F)            publish time (%globaltimer ns) of each flag slot
  *   [F, 2F)           earliest time a consumer's acquire of the slot
  *                     succeeded (atomicMin; the caller fills this range
@@ -326,8 +333,10 @@ opw_status opw_ag_gemm_noalloc(const opw_symm* symm, size_t a_off, int64_t M_r, 
 
 /* ---------------------------------------------------------------- GEMM-RS */
 
-/* Flag slots for GEMM-RS outputs: 128x128 tiles of each rank's [M/R, N]
- * block, slot (j * (M/R/128) + mt) * ceil(N/128) + nt.  -1 if invalid. */
+/* Flag slots for GEMM-RS outputs ("GEMM and ReduceScatter Overlapping" step
+ * 2, a signal after each tile is computed): 128x128 tiles of each rank's
+ * [M/R, N] block, slot (j * (M/R/128) + mt) * ceil(N/128) + nt.  -1 if
+ * invalid. */
 int64_t opw_rs_num_flags(int32_t R, int64_t M, int64_t N);
 
 /*
