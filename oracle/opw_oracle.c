@@ -368,7 +368,9 @@ int64_t opw_oracle_swizzle_row(int64_t pid_m, int64_t rank, int64_t tiles_per_pe
  * a persistent grid of G consumers.  Every consumer follows one order of the
  * tiles: row tiles in groups of group_rows consecutive rows, the column index
  * outermost inside a group (so consumers working at the same time share the
- * column tiles of B), and every row tile pid_m renamed so that the PE starts
+ * column tiles of B) and running backwards in every second group (so a group
+ * starts on the column tiles the previous one used last), and every row tile
+ * pid_m renamed so that the PE starts
  * on its own rows and then moves on to the other ranks' rows.  With visit ==
  * NULL the renaming is the page's formula swizzle_row(pid_m, rank,
  * tiles_per_pe, T_M): rank+1's rows next, then rank+2's, ... (the order a
@@ -389,7 +391,9 @@ int64_t opw_oracle_consumer_order(int64_t T_M, int64_t T_N, int64_t G, int64_t c
         const int64_t rows = T_M - first < group_rows ? T_M - first : group_rows;
         const int64_t local = pos - first * T_N;
         const int64_t pid_m = first + local % rows;
-        const int64_t pid_n = local / rows;
+        const int64_t col = local / rows;
+        /* successive groups sweep the columns in alternating directions */
+        const int64_t pid_n = (first / group_rows) % 2 == 0 ? col : T_N - 1 - col;
         const int64_t m = visit == NULL
                               ? opw_oracle_swizzle_row(pid_m, rank, tiles_per_pe, T_M)
                               : visit[pid_m / tiles_per_pe] * tiles_per_pe + pid_m % tiles_per_pe;

@@ -309,6 +309,14 @@ def test_consumer_order_is_a_partition_starting_at_own_rows(T_M, T_N, G, GM, ran
     for o in orders:
         rows = [((q // T_N) - rank * tpp) % T_M for q in o]
         assert [r // GM for r in rows] == sorted(r // GM for r in rows)
+    # the whole order (position p is consumer p mod G's (p div G)-th tile):
+    # inside a row group the columns never go backwards in even groups and
+    # never forwards in odd ones
+    full = [orders[pos % G][pos // G] for pos in range(T_M * T_N)]
+    for pos0 in range(0, T_M * T_N, GM * T_N):
+        g = pos0 // (GM * T_N)
+        cols = [q % T_N for q in full[pos0:pos0 + GM * T_N]]
+        assert cols == (sorted(cols) if g % 2 == 0 else sorted(cols, reverse=True))
     # the rank visit order of a ring (own rank, then rank+1, rank+2, ...) is
     # the page's formula, whenever the row tiles split evenly over the ranks
     if T_M % tpp == 0:
