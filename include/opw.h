@@ -152,12 +152,19 @@ typedef struct {
                                 same slots (same R and tile geometry): slots an
                                 earlier launch did not publish hold older epochs. */
 
-#define OPW_SCHED_READY   0  /* dynamic (default): CTAs claim output tiles from a
-                                device counter in the order their rows are
-                                published, so every consumer starts on the tiles
-                                that are ready first */
-#define OPW_SCHED_SWIZZLE 1  /* static: CTA c starts on home rank c mod R and
-                                rotates ("Threadblock Swizzling") */
+/* Both schedules walk one order of the 256x256 output tiles: pair rows in
+ * groups (8 when B is over 64 MiB, else 1), the column index outermost in a
+ * group and running backwards in every second group; rows renamed so that the
+ * PE the GPU plays (opts.local_rank, rank 0 when -1) starts on its own rows,
+ * then the other ranks' rows in publish order: with the default ring publish
+ * order that is "Threadblock Swizzling"'s pid_m = (pid_m + rank *
+ * tiles_per_pe) % total_tiles with tiles_per_pe = M_r / 256. */
+#define OPW_SCHED_READY   0  /* dynamic (default): CTA pairs claim positions of
+                                that order from a device counter, so every
+                                consumer starts on the tiles that are ready
+                                first */
+#define OPW_SCHED_SWIZZLE 1  /* static: CTA pair c takes positions c, c + G,
+                                c + 2G, ... of that order (G pairs) */
 
 #define OPW_ROLE_FUSED    0  /* producer warps and consumer warps together */
 #define OPW_ROLE_PRODUCER 1  /* only the gather + publish (for overlap timing) */
@@ -191,7 +198,8 @@ typedef struct {
     const int32_t* publish_perm;  /* host [R] or NULL: rank publish_perm[i] is published
                                      i-th, and none of its tiles before every tile of
                                      rank publish_perm[i-1] is published.  NULL: ranks
-                                     interleaved row block by row block. */
+                                     in ring order after local_rank (local_rank + 1,
+                                     + 2, ...), the local rank's own shard last. */
     const uint32_t* delay_ns;     /* host [R] or NULL: no copy of rank r starts earlier
                                      than delay_ns[r] after its CTA started */
     uint64_t* trace_dev;          /* device [opw_ag_trace_words()] or NULL; see below */

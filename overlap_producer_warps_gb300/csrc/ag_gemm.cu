@@ -14,7 +14,7 @@
 //   warp 0     loader (both CTAs): takes tiles from the on-chip tile queue and
 //              TMA-loads this CTA's half of their A k-blocks (from the gathered
 //              buffer G, or in place from the local rank's own shard) and B
-//              k-blocks into a 5-stage ring; the bytes of both halves complete
+//              k-blocks into a 6-stage ring; the bytes of both halves complete
 //              on the even CTA's `full` barrier.
 //   warp 1     MMA (even CTA only): one thread issues the pair's tcgen05.mma
 //              (bf16 x bf16 -> fp32) into a double-buffered TMEM accumulator
