@@ -338,3 +338,37 @@ def test_row_add_and_tile_set_do_not_mix_without_reset(api):
     assert sig.status()[0] == api.OK
     _, C_ref = prob.oracle_full()
     assert_gemm_close(host_bits(prob.C), C_ref)
+
+
+@pytest.mark.parametrize("perm", [None, (3, 1, 0, 2)])
+def test_launch_behind_another_streams_gemm(api, perm):
+    """The launch needs no co-residency: started while another stream's GEMMs
+    still hold the SMs, its CTAs are placed as SMs free up, so producers and
+    consumers start at different times (the trace records how far apart).
+    Neither kernel waits on the other; the result must still be the oracle's
+    and every flag the epoch."""
+    R, M_r, K, N = 4, 1024, 1024, 2048
+    d = inputs.ag_inputs(_cfg(R, M_r, K, N), seed=91)
+    prob = AgProblem(d)
+    F = api.ag_num_flags(R, M_r, K)
+    sig = api.Signal(F)
+    words = api.ag_trace_words(R, M_r, N, K)
+    trace = torch.full((words,), -1, dtype=torch.int64, device="cuda")
+    big = torch.randn(8192, 8192, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(big)
+    other = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(other):
+        for _ in range(4):
+            torch.matmul(big, big, out=out)
+    e = sig.next_epoch()
+    prob.run(api, sig, e, api.make_opts(trace=trace, publish_perm=perm))
+    torch.cuda.synchronize()
+    assert sig.status()[0] == api.OK
+    assert np.all(sig.flags().cpu().numpy() == e)
+    G_ref, C_ref = prob.oracle_full()
+    assert np.array_equal(host_bits(prob.G), G_ref)
+    assert_gemm_close(host_bits(prob.C), C_ref)
+    grid = torch.cuda.get_device_properties(0).multi_processor_count
+    starts = _trace_views(api, prob, trace, grid)["cta_start"].astype(np.float64)
+    print(f"CTA start spread: {(starts.max() - starts.min()) / 1e3:.1f} us")
