@@ -565,6 +565,8 @@ def ag_config_results(api, torch, name, peak_tflops, reps):
 
     fns = {"fused": w.launch,
            "swizzle": lambda: w.launch(schedule=api.SCHED_SWIZZLE),
+           # every tile, the consumer's own shard's included, read from G after its flag
+           "no_local": lambda: w.launch(local_rank=-1),
            # every consumer waits for the whole gather before its first tile
            "serial": lambda: w.launch(sync_mode=api.SYNC_SERIAL),
            "row_add": fused_row_add,
@@ -598,6 +600,7 @@ def ag_config_results(api, torch, name, peak_tflops, reps):
         "swizzle_schedule_tflops": fl / med["swizzle"] / 1e9,
         "serial_sync_tflops": fl / med["serial"] / 1e9,
         "row_add_signal_tflops": fl / med["row_add"] / 1e9,
+        "no_local_shard_tflops": fl / med["no_local"] / 1e9,
         "unfused_copy_then_gemm_tflops": fl / med["unfused"] / 1e9,
         "cublas_gemm_only_tflops": fl / med["gemm_only"] / 1e9,
         "fused_vs_cublas_gemm_only": med["gemm_only"] / med["fused"],
@@ -648,8 +651,15 @@ def rs_config_results(api, torch, peak_tflops, reps):
     A_cat = torch.cat(A, dim=1)
     B_cat = torch.cat(Bs, dim=0)
     C_cat = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    recv = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+
+    def rs_consume():
+        api.gemm_rs_consume(heap, d["rank_off"], d["a_off"], d["b_off"], d["out_off"], M, N, K_r,
+                            recv, sig, sig.next_epoch())
+
     t = time_interleaved(torch, {
-        "fused": rs, "gemm_leg_only": lambda: rs(api.ROLE_PRODUCER),
+        "fused": rs, "with_receiving_side": rs_consume,
+        "gemm_leg_only": lambda: rs(api.ROLE_PRODUCER),
         "scatter_leg_only": lambda: rs(api.ROLE_CONSUMER), "unfused": unfused_rs,
         "gemm_only": lambda: torch.matmul(A_cat, B_cat, out=C_cat)},
         rounds=max(1, reps // 4), per_round=4)
@@ -665,6 +675,7 @@ def rs_config_results(api, torch, peak_tflops, reps):
     return {"fused_tflops": fl / med["fused"] / 1e9,
             "fused_tflops_best": fl / t["fused"]["min"] / 1e9,
             "pct_of_peak": fl / med["fused"] / 1e9 / peak_tflops,
+            "with_receiving_side_tflops": fl / med["with_receiving_side"] / 1e9,
             "unfused_partials_then_sum_tflops": fl / med["unfused"] / 1e9,
             "unfused_partials": mm32_name,
             "cublas_single_gemm_tflops": fl / med["gemm_only"] / 1e9,
