@@ -36,6 +36,9 @@
 // waited for; its producer copies still fill G, after every other rank's.
 //   warps 4-7  epilogue (both CTAs): tcgen05.ld -> bf16 (round to nearest
 //              even) -> swizzled shared memory -> TMA store of C.
+// With the gather alone (OPW_ROLE_PRODUCER) there are no consumer roles:
+// warps 0-6 of every CTA are producers, each with staging buffers of its own
+// in the shared memory the ring and the epilogue would use.
 // Every wait is bounded: on timeout the kernel latches an error in the
 // signal object's status word, drains its own in-flight copies and MMAs,
 // frees TMEM and returns.  Cluster barriers bracket the kernel, so neither CTA
@@ -672,14 +675,16 @@ __device__ __forceinline__ void publish_tile(const AgParams& p, const ErrCtx& ec
     if (p.trace != nullptr) p.trace[slot] = t_pub;
 }
 
-// Warp 2 of every CTA.  Flag tiles are claimed one at a time from a device
-// counter, in publish order, by whichever producer warps are running, so no
-// wait anywhere in the grid depends on a CTA that has not started: the launch
-// needs no co-residency guarantee.  A tile is copied 32 rows at a time: TMA
-// loads of A_r rows into the staging buffers, then a TMA store of each into G
-// as it lands.  The next tile's loads are issued before the previous tile's
-// stores are waited for and its flag published, and the next claim is made
-// while the current tile is in flight.
+// A producer warp: warp 2 of every CTA in the fused kernel, or every warp
+// that fits in the idle shared memory when the gather runs alone.  Flag
+// tiles are claimed one at a time from a device counter, in publish order, by
+// whichever producer warps are running, so no wait anywhere in the grid
+// depends on a CTA that has not started: the launch needs no co-residency
+// guarantee.  A tile is copied 32 rows at a time: TMA loads of A_r rows into
+// the staging buffers, then a TMA store of each into G as it lands, with a
+// buffer refilled as soon as its store has read it.  The next tile's loads
+// are issued before the previous tile's stores are waited for and its flag
+// published, and the next claim is made while the current tile is in flight.
 // buf0 / gfull: this warp's nb staging buffers (GATHER_BUF_BYTES each) and
 // their barriers.
 __device__ void run_gather(const AgParams& p, uint8_t* buf0, uint64_t* gfull, int nb,
