@@ -16,9 +16,9 @@
 //              buffer G, or in place from the local rank's own shard) and B
 //              k-blocks into a 6-stage ring; the bytes of both halves complete
 //              on the even CTA's `full` barrier.
-//   warp 1     MMA (even CTA only): one thread issues the pair's tcgen05.mma
-//              (bf16 x bf16 -> fp32) into a double-buffered TMEM accumulator
-//              (2 x 128 lanes x 256 columns in each CTA).
+//   warp 1     MMA (even CTA only): lane 0 alone issues the pair's
+//              tcgen05.mma (bf16 x bf16 -> fp32) into a double-buffered TMEM
+//              accumulator (2 x 128 lanes x 256 columns in each CTA).
 //   warp 2     gather producer (every CTA): claims flag tiles of A_r from a
 //              device counter in publish order, TMA-copies each into G through
 //              shared memory, waits for the copy to complete, and publishes the
@@ -342,6 +342,18 @@ __device__ __forceinline__ int pop_tile(AgCtrl* ctrl, const ErrCtx& ec, uint32_t
     return q;
 }
 
+// pop_tile for a single thread (the MMA issuer): the same wait, read and
+// release, with no warp to synchronise.
+__device__ __forceinline__ int pop_tile_thread(AgCtrl* ctrl, const ErrCtx& ec, uint32_t& tq,
+                                               uint32_t& tqphase)
+{
+    if (!wait_bar_cluster(&ctrl->tq_full[tq], tqphase, ec, SITE_TILE_QUEUE)) return -2;
+    const int q = reinterpret_cast<volatile int32_t*>(ctrl->tile_q)[tq];
+    mbar_arrive(&ctrl->tq_empty[tq]);
+    if (++tq == TILE_Q) { tq = 0; tqphase ^= 1u; }
+    return q;
+}
+
 // Odd CTA, warp 3: for each queue slot in turn, wait until the odd CTA's
 // readers have taken it (tq_fwd), then free it on the even CTA's tq_empty
 // with one cluster-scope release arrive.  That release is cumulative: it
@@ -474,18 +486,27 @@ __device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
 
 // ------------------------------------------------------------------ MMA
 
-// Even CTA, warp 1.
+// Even CTA, warp 1, lane 0 alone.  The tensor pipe takes an MMA only a
+// little ahead of executing it, so whatever this thread does between one
+// k-block's MMAs and the next lands on the pipe's critical path: one thread
+// with no per-k-block warp synchronisation, stage counters instead of
+// divisions, and descriptors stepped by addition (the start-address field
+// is the shared address >> 4) kept the k-block at about 515 cycles against
+// 570 for the same loop run by a whole warp.
 __device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t tmem,
                         const ErrCtx& ec)
 {
-    const uint32_t lane = lane_id();
     const int KB = p.K / BK;
-    const uint32_t a_base = smem_u32(smem + OFF_A);
-    const uint32_t b_base = smem_u32(smem + OFF_B);
+    // A: K-major, rows 128 B apart, 8-row groups 1024 B apart; k steps of 16
+    //    elements advance 32 B inside the swizzled row.
+    const uint64_t a_desc0 = sdesc_sw128(smem_u32(smem + OFF_A), 16, 1024);
+    // B: N-major, 64-column chunks 8 KiB apart (LBO), 8-row K groups 1024 B
+    //    apart (SBO); k steps of 16 rows advance 2 KiB.
+    const uint64_t b_desc0 = sdesc_sw128(smem_u32(smem + OFF_B), B_CHUNK_BYTES, 1024);
     uint32_t stage = 0, sphase = 0, acc = 0, aphase = 0, tq = 0, tqphase = 0;
     bool ok = true;
     while (ok) {
-        const int q = pop_tile(ctrl, ec, tq, tqphase, 0u);
+        const int q = pop_tile_thread(ctrl, ec, tq, tqphase);
         if (q < 0) break;
 
         // both CTAs' epilogues have read this accumulator
@@ -495,32 +516,21 @@ __device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t
         for (int kb = 0; kb < KB; ++kb) {
             if (!wait_bar(&ctrl->full[stage], sphase, ec, SITE_MMA_FULL)) { ok = false; break; }
             tc_fence_after();
-            if (lane == 0) {
-                const uint32_t as = a_base + stage * A_STAGE_BYTES;
-                const uint32_t bs = b_base + stage * B_HALF_BYTES;
+            const uint64_t ad = a_desc0 + stage * (A_STAGE_BYTES >> 4);
+            const uint64_t bd = b_desc0 + stage * (B_HALF_BYTES >> 4);
 #pragma unroll
-                for (int k = 0; k < BK / UMMA_K; ++k) {
-                    // A: K-major, rows 128 B apart, 8-row groups 1024 B apart;
-                    //    k steps of 16 elements advance 32 B inside the swizzled row.
-                    const uint64_t ad = sdesc_sw128(as + k * (UMMA_K * 2), 16, 1024);
-                    // B: N-major, 64-column chunks 8 KiB apart (LBO), 8-row K groups
-                    //    1024 B apart (SBO); k steps of 16 rows advance 2 KiB.
-                    const uint64_t bd = sdesc_sw128(bs + k * (UMMA_K * 128), B_CHUNK_BYTES, 1024);
-                    mma_bf16_pair(d, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
-                }
-                mma_commit_pair(&ctrl->empty[stage], 0x3);  // frees both CTAs' stage when done
-            }
-            __syncwarp();
+            for (int k = 0; k < BK / UMMA_K; ++k)
+                mma_bf16_pair(d, ad + k * ((UMMA_K * 2) >> 4), bd + k * ((UMMA_K * 128) >> 4), IDESC,
+                              (kb | k) != 0 ? 1u : 0u);
+            mma_commit_pair(&ctrl->empty[stage], 0x3);  // frees both CTAs' stage when done
             if (++stage == AG_STAGES) { stage = 0; sphase ^= 1u; }
         }
         if (!ok) break;
-        if (lane == 0) mma_commit_pair(&ctrl->tmem_full[acc], 0x3);
-        __syncwarp();
+        mma_commit_pair(&ctrl->tmem_full[acc], 0x3);
         if (++acc == 2) { acc = 0; aphase ^= 1u; }
     }
     // Every MMA issued must complete before TMEM is released.
-    if (lane == 0) mma_commit_pair(&ctrl->mma_done, 0x1);
-    __syncwarp();
+    mma_commit_pair(&ctrl->mma_done, 0x1);
     drain_bar(&ctrl->mma_done, 0, ec);
 }
 
@@ -890,7 +900,7 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
         if (warp == 0) {
             if (consumer) run_loader(p, smem, ctrl, ec, crank);
         } else if (warp == 1) {
-            if (consumer && crank == 0) run_mma(p, smem, ctrl, tmem, ec);
+            if (consumer && crank == 0 && lane_id() == 0) run_mma(p, smem, ctrl, tmem, ec);
         } else if (warp == 2) {
             if (producer)
                 run_gather(p, smem + OFF_GATHER, ctrl->gfull, GATHER_BUFS, ec, t_start);

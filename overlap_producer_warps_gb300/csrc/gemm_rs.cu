@@ -188,16 +188,22 @@ __device__ void rs_loader(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, const 
             if (filled & (1u << st)) drain_bar(&ctrl->full[st], (last_par >> st) & 1u, ec);
 }
 
-// Even CTA only.
+// Even CTA, warp 1, lane 0 alone: the MMA issue loop (one thread, no warp
+// synchronisation per stage, descriptors stepped by addition), since the
+// issuing thread's work between one stage's MMAs and the next is on the
+// tensor pipe's critical path.
 __device__ void rs_mma(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32_t tmem,
                        const ErrCtx& ec)
 {
     if (p.role == OPW_ROLE_CONSUMER) return;
-    const uint32_t lane = lane_id();
     const PairSched ps = pair_sched(p);
     const int KB = (p.K_r + RBK - 1) / RBK;
-    const uint32_t a_base = smem_u32(smem + OFF_A);
-    const uint32_t b_base = smem_u32(smem + OFF_B);
+    // A: K-major, two 128-row x 64-K atoms 16 KiB apart; k steps of 16
+    //    elements advance 32 B inside an atom's swizzled rows.
+    const uint64_t a_desc0 = sdesc_sw128(smem_u32(smem + OFF_A), 16, 1024);
+    // B: N-major, 64-column chunks of 128 K-rows 16 KiB apart (LBO), 8-row K
+    //    groups 1024 B apart (SBO); k steps advance 2 KiB.
+    const uint64_t b_desc0 = sdesc_sw128(smem_u32(smem + OFF_B), RB_CHUNK, 1024);
     uint32_t stage = 0, sphase = 0, acc = 0, aphase = 0;
     bool ok = true;
     for (int i = 0; i < ps.nt && ok; ++i) {
@@ -210,33 +216,21 @@ __device__ void rs_mma(const RsParams& p, uint8_t* smem, RsCtrl* ctrl, uint32_t 
             for (int kb = 0; kb < KB; ++kb) {
                 if (!wait_bar(&ctrl->full[stage], sphase, ec, SITE_MMA_FULL)) { ok = false; break; }
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t as = a_base + stage * RA_STAGE;
-                    const uint32_t bs = b_base + stage * B_HALF_BYTES;
+                const uint64_t ad = a_desc0 + stage * (RA_STAGE >> 4);
+                const uint64_t bd = b_desc0 + stage * (B_HALF_BYTES >> 4);
 #pragma unroll
-                    for (int k = 0; k < RBK / UMMA_K; ++k) {
-                        // A: K-major, two 128-row x 64-K atoms 16 KiB apart; k steps of
-                        //    16 elements advance 32 B inside an atom's swizzled rows.
-                        const uint64_t ad = sdesc_sw128(
-                            as + (k >> 2) * (RA_STAGE / 2) + (k & 3) * (UMMA_K * 2), 16, 1024);
-                        // B: N-major, 64-column chunks of 128 K-rows 16 KiB apart (LBO),
-                        //    8-row K groups 1024 B apart (SBO); k steps advance 2 KiB.
-                        const uint64_t bd = sdesc_sw128(bs + k * (UMMA_K * 128), RB_CHUNK, 1024);
-                        mma_bf16_pair(d, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
-                    }
-                    mma_commit_pair(&ctrl->empty[stage], 0x3);  // both CTAs' stage is free
-                }
-                __syncwarp();
+                for (int k = 0; k < RBK / UMMA_K; ++k)
+                    mma_bf16_pair(d, ad + ((k >> 2) * (RA_STAGE / 2) + (k & 3) * (UMMA_K * 2)) / 16,
+                                  bd + k * ((UMMA_K * 128) >> 4), IDESC, (kb | k) != 0 ? 1u : 0u);
+                mma_commit_pair(&ctrl->empty[stage], 0x3);  // both CTAs' stage is free
                 if (++stage == RS_STAGES) { stage = 0; sphase ^= 1u; }
             }
             if (!ok) break;
-            if (lane == 0) mma_commit_pair(&ctrl->tmem_full[acc], 0x3);  // partial P_r is ready
-            __syncwarp();
+            mma_commit_pair(&ctrl->tmem_full[acc], 0x3);  // partial P_r is ready
             if (++acc == 2) { acc = 0; aphase ^= 1u; }
         }
     }
-    if (lane == 0) mma_commit_pair(&ctrl->mma_done, 0x1);
-    __syncwarp();
+    mma_commit_pair(&ctrl->mma_done, 0x1);
     drain_bar(&ctrl->mma_done, 0, ec);
 }
 
@@ -434,7 +428,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
         if (warp == 0) {
             rs_loader(p, smem, ctrl, ec, crank);
         } else if (warp == 1) {
-            if (crank == 0) rs_mma(p, smem, ctrl, tmem, ec);
+            if (crank == 0 && lane_id() == 0) rs_mma(p, smem, ctrl, tmem, ec);
         } else if (warp == 3) {
             rs_receive(p, ec, crank);
         } else if (warp >= 4) {

@@ -430,6 +430,32 @@ __device__ __forceinline__ bool aborted(const ErrCtx& e)
     return *e.cta_abort != 0 || ld_relaxed_s32(e.status) != 0;
 }
 
+// A wait on an on-chip barrier looks at the grid-wide status word (a global
+// load, several hundred cycles) only once it has lasted this long.  Waits on
+// the k-block pipeline last well under it, so the loader and the MMA thread
+// never leave the SM while they poll: a poll stuck behind that load used to
+// react late to a stage that had just landed or been freed, and the k-block
+// cadence fell from about 530 to about 700 cycles.
+constexpr uint64_t GRID_POLL_AFTER_NS = 20000;
+
+// One round of the bounded-wait checks (every 16 polls).  True when the
+// wait must give up: this CTA has aborted (shared memory, checked every
+// round), another part of the grid has latched an error (the global status
+// word, read only after GRID_POLL_AFTER_NS), or the wait has run past
+// `limit_ns` (latches OPW_ERR_TIMEOUT tagged `who`).
+__device__ __forceinline__ bool wait_must_stop(const ErrCtx& e, uint64_t t0, uint32_t i,
+                                               uint64_t limit_ns, int32_t who)
+{
+    if (*e.cta_abort != 0) return true;
+    const uint64_t dt = globaltimer() - t0;
+    if (dt > GRID_POLL_AFTER_NS && (i & 255u) == 0 && ld_relaxed_s32(e.status) != 0) return true;
+    if (dt > limit_ns) {
+        raise_error(e, OPW_ERR_TIMEOUT, -1, who);
+        return true;
+    }
+    return false;
+}
+
 // Bounded mbarrier wait.  Returns false (after latching an error) if the
 // phase does not complete in time or another part of the grid has already
 // failed.  `who` tags the waiting role in the status word.  On-chip barriers
@@ -443,13 +469,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const E
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 15u) == 0) {
-            if (aborted(e)) return false;
-            if (globaltimer() - t0 > 4 * e.timeout_ns) {
-                raise_error(e, OPW_ERR_TIMEOUT, -1, who);
-                return false;
-            }
-        }
+        if ((i & 15u) == 0 && wait_must_stop(e, t0, i, 4 * e.timeout_ns, who)) return false;
     }
 }
 
@@ -461,13 +481,7 @@ __device__ __forceinline__ bool wait_bar_cluster(uint64_t* bar, uint32_t parity,
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((i & 15u) == 0) {
-            if (aborted(e)) return false;
-            if (globaltimer() - t0 > 4 * e.timeout_ns) {
-                raise_error(e, OPW_ERR_TIMEOUT, -1, who);
-                return false;
-            }
-        }
+        if ((i & 15u) == 0 && wait_must_stop(e, t0, i, 4 * e.timeout_ns, who)) return false;
     }
 }
 
