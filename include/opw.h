@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define OPW_ABI_VERSION 1
+#define OPW_ABI_VERSION 2
 #define OPW_MAX_RANKS 8
 
 /* ---------------------------------------------------------------- status */
@@ -152,7 +152,8 @@ typedef struct {
                                 same slots (same R and tile geometry): slots an
                                 earlier launch did not publish hold older epochs. */
 
-/* Both schedules walk one order of the 256x256 output tiles: pair rows in
+/* Both schedules walk one order of the 256 x TN output tiles (TN = the pair
+ * tile width of the launch, 256 or 512; see opw_ag_tile_n): pair rows in
  * groups (8 when B is over 64 MiB, else 1), the column index outermost in a
  * group and running backwards in every second group; rows renamed so that the
  * PE the GPU plays (opts.local_rank, rank 0 when -1) starts on its own rows,
@@ -209,6 +210,9 @@ typedef struct {
     int32_t local_rank;           /* AG-GEMM: the logical rank the consumer plays, whose own
                                      shard is local (default 0); -1: none.  Other calls
                                      accept 0 or -1 and ignore it.  See opw_ag_gemm. */
+    int32_t tile_n;               /* AG-GEMM: output columns of a pair tile, 256 or 512;
+                                     0 (default) = the library's choice for the shape and
+                                     grid (opw_ag_tile_n).  Other calls require 0. */
 } opw_opts;
 
 /* Fill *o with the defaults (all fields 0 / NULL). */
@@ -239,17 +243,35 @@ int64_t opw_ag_num_row_counters(int32_t R, int64_t M_r, int64_t K);
  *   [F, 2F)           earliest time a consumer's acquire of the slot
  *                     succeeded (atomicMin; the caller fills this range
  *                     with all-ones bits before the launch)
- *   [2F, 2F+T)        per 256x256 output tile q = (row / 256) * ceil(N/256)
- *                     + col / 256: (pair << 32) | visit position, where
+ *   [2F, 2F+T)        per 256 x TN output tile q = (row / 256) * ceil(N/TN)
+ *                     + col / TN: (pair << 32) | visit position, where
  *                     pair c is the CTA pair 2c, 2c+1
  *   [2F+T, 2F+2T)     per output tile: time its pair's scheduler claimed it
  *                     (before its first flag acquire)
  *   [2F+2T, 2F+2T+G)  per CTA: start time
- * with F = opw_ag_num_flags(), T = ceil(M/256)*ceil(N/256), G = grid size
- * (at most OPW_TRACE_MAX_CTAS words are reserved).
+ * with F = opw_ag_num_flags(), T = ceil(M/256)*ceil(N/TN), TN the launch's
+ * pair tile width (opw_ag_tile_n), G = grid size (at most OPW_TRACE_MAX_CTAS
+ * words are reserved).  opw_ag_trace_words() sizes the buffer for TN = 256,
+ * which also covers TN = 512.
  */
 #define OPW_TRACE_MAX_CTAS 1024
 int64_t opw_ag_trace_words(int32_t R, int64_t M_r, int64_t N, int64_t K);
+
+/*
+ * Output columns TN of the pair tiles an opw_ag_gemm (or opw_ag_gemm_noalloc)
+ * launch with these sizes and options uses on the current device: opts->tile_n
+ * when it is set, else the library's choice.  A 256 x 512 pair tile reads a
+ * quarter less operand data from L2 per FLOP than a 256 x 256 one (a lower
+ * on-chip power draw, so a higher clock under the power cap), but holds its
+ * one 512-column TMEM accumulator through the epilogue; the library takes it
+ * when its whole waves of tiles, at 1.93 times the time of a 256-wide wave,
+ * are shorter than the 256-wide waves.  This is a refinement of the pages'
+ * "one program per output tile" ("AllGather and GEMM Overlapping"), with no
+ * change to the results: every output element sums the same products in the
+ * same order.  Returns 256, 512, or -1 (invalid arguments, or no CUDA device
+ * to size the grid for when opts->tile_n is 0).  opts may be NULL.
+ */
+int32_t opw_ag_tile_n(int32_t R, int64_t M_r, int64_t N, const opw_opts* opts);
 
 /*
  * AllGather -> GEMM ("AllGather and GEMM Overlapping"):
@@ -273,9 +295,9 @@ int64_t opw_ag_trace_words(int32_t R, int64_t M_r, int64_t N, int64_t K);
  * never wait on its flags, and they take its tiles first.  Its tiles are still
  * copied into G (after every other rank's) and published.  With local_rank =
  * -1 every tile is read from G after its flag.
- * Consumers, in CTA pairs working on 256x256 output tiles, acquire each flag
- * (>= epoch) before their TMA loads read that tile of G, then run tcgen05
- * cta_group::2 MMAs with TMEM accumulators.  After the launch every flag slot
+ * Consumers, in CTA pairs working on 256 x TN output tiles (opw_ag_tile_n),
+ * acquire each flag (>= epoch) before their TMA loads read that tile of G,
+ * then run tcgen05 cta_group::2 MMAs with TMEM accumulators.  After the launch every flag slot
  * holds `epoch` and G is bit-identical to the concatenation.
  *
  * Producer warps claim flag tiles from a device counter in publish order, so

@@ -51,7 +51,7 @@ class Opts(ctypes.Structure):
                 ("delay_ns", ctypes.POINTER(ctypes.c_uint32)),
                 ("trace_dev", ctypes.c_void_p), ("fault_kind", ctypes.c_int32),
                 ("fault_arg", ctypes.c_int32), ("signal_mode", ctypes.c_int32),
-                ("local_rank", ctypes.c_int32)]
+                ("local_rank", ctypes.c_int32), ("tile_n", ctypes.c_int32)]
 
 
 _vp = ctypes.c_void_p
@@ -72,6 +72,8 @@ SIGNATURES = {
                                                  ctypes.c_int64]),
     "opw_ag_trace_words": (ctypes.c_int64, [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
                                             ctypes.c_int64]),
+    "opw_ag_tile_n": (ctypes.c_int32, [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
+                                       ctypes.POINTER(Opts)]),
     "opw_ag_gemm": (ctypes.c_int32, [ctypes.POINTER(Symm), ctypes.c_size_t, ctypes.c_int64,
                                      ctypes.c_int64, ctypes.c_int64, _vp, _vp, _vp, _vp,
                                      ctypes.c_uint64, ctypes.POINTER(Opts), _vp]),
@@ -199,7 +201,7 @@ class Signal:
 
 def make_opts(timeout_ns=0, sync_mode=SYNC_OVERLAP, schedule=SCHED_READY, role=ROLE_FUSED,
               num_ctas=0, publish_perm=None, delay_ns=None, trace=None, fault_kind=FAULT_NONE,
-              fault_arg=0, signal_mode=SIGNAL_TILE_SET, local_rank=0):
+              fault_arg=0, signal_mode=SIGNAL_TILE_SET, local_rank=0, tile_n=0):
     """Build an Opts struct; array arguments are kept alive on the struct."""
     o = Opts()
     lib().opw_opts_default(ctypes.byref(o))
@@ -223,6 +225,7 @@ def make_opts(timeout_ns=0, sync_mode=SYNC_OVERLAP, schedule=SCHED_READY, role=R
     o.fault_arg = int(fault_arg)
     o.signal_mode = int(signal_mode)
     o.local_rank = int(local_rank)
+    o.tile_n = int(tile_n)
     o._keep = keep
     return o
 
@@ -252,6 +255,13 @@ def ag_num_row_counters(R: int, M_r: int, K: int) -> int:
 
 def ag_trace_words(R: int, M_r: int, N: int, K: int) -> int:
     return int(lib().opw_ag_trace_words(R, M_r, N, K))
+
+
+def ag_tile_n(R: int, M_r: int, N: int, opts=None) -> int:
+    """Pair tile columns (256 or 512) an AG-GEMM launch with these sizes and
+    options uses on the current device (-1 on error)."""
+    return int(lib().opw_ag_tile_n(int(R), int(M_r), int(N),
+                                   ctypes.byref(opts) if opts is not None else None))
 
 
 def rs_num_flags(R: int, M: int, N: int) -> int:

@@ -51,20 +51,45 @@
 namespace opw {
 namespace {
 
-// A 6-stage ring with 2 gather staging buffers fits the budget (225 KiB);
-// against 5 stages with 4 buffers it was 1.3-2.2 % faster fused on every
-// layer in a burst, about even under the power cap, and its gather alone
-// 15 % slower (hidden in the fused kernel).
-constexpr int AG_STAGES = 6;
 constexpr int GATHER_BUFS = 2;    // the fused kernel's producer staging buffers
 constexpr int PROD_BUFS = 4;      // per producer warp when the gather runs alone
-constexpr int HALF_N = BN / 2;                  // B columns held by each CTA
+constexpr int HALF_N = BN / 2;                  // B columns of one MMA held by each CTA
 constexpr int B_HALF_BYTES = BK * HALF_N * 2;   // 16 KiB: 2 chunks of 64 columns
-constexpr uint32_t PAIR_TX_BYTES = 2u * (A_STAGE_BYTES + B_HALF_BYTES);
+
+// Pair tiles are 256 x (256 * NW).
+//   NW = 1: one N = 256 MMA per k step into a double-buffered TMEM accumulator
+//           (2 x 256 columns), so the epilogue of one tile overlaps the MMAs of
+//           the next; a 6-stage ring of 32 KiB stages.  With 2 gather staging
+//           buffers it fits the budget (225 KiB); against 5 stages with 4
+//           buffers it was 1.3-2.2 % faster fused in a burst.
+//   NW = 2: two N = 256 MMAs per k step (B columns 0-255 and 256-511 of the
+//           tile) into one 512-column accumulator; a 4-stage ring of 48 KiB
+//           stages (4 x 1024 cycles of MMA in flight).  A CTA reads a quarter
+//           less operand data from L2 per FLOP; the epilogue no longer overlaps
+//           the next tile's MMAs.  In a probe GEMM with this epilogue, random
+//           operands and whole waves it ran 3.7 % faster in a burst and 5-8 %
+//           faster under the power cap, where the lower on-chip traffic bought
+//           a 9 % higher SM clock.
+// The host picks the width per launch (opts.tile_n, or from the wave counts).
+template <int NW>
+struct Shape {
+    static constexpr int STAGES = NW == 1 ? 6 : 4;
+    static constexpr int B_STAGE = NW * B_HALF_BYTES;   // this CTA's B bytes per stage
+    static constexpr int OFF_B = STAGES * A_STAGE_BYTES;
+    static constexpr int RING_END = OFF_B + STAGES * B_STAGE;
+    static constexpr uint32_t TX = 2u * (A_STAGE_BYTES + B_STAGE);  // both CTAs' bytes per stage
+    static constexpr int ACCS = NW == 1 ? 2 : 1;        // TMEM accumulators
+    static constexpr int CHUNKS = NW * BN / 64;         // 64-column epilogue chunks per tile
+};
+static_assert(Shape<1>::RING_END == Shape<2>::RING_END, "both rings fill the same space");
+static_assert(Shape<1>::OFF_B % 1024 == 0 && Shape<2>::OFF_B % 1024 == 0 &&
+                  A_STAGE_BYTES % 1024 == 0 && B_HALF_BYTES % 1024 == 0,
+              "swizzled stages must be 1024-byte aligned");
+constexpr int AG_STAGES_MAX = 6;
 
 struct AgCtrl {
-    uint64_t full[AG_STAGES];   // even CTA: both halves of a stage have landed
-    uint64_t empty[AG_STAGES];  // each CTA: the pair MMA is done with its stage
+    uint64_t full[AG_STAGES_MAX];   // even CTA: both halves of a stage have landed
+    uint64_t empty[AG_STAGES_MAX];  // each CTA: the pair MMA is done with its stage
     uint64_t tmem_full[2];      // each CTA: an accumulator is complete in its TMEM
     uint64_t tmem_empty[2];     // even CTA: both CTAs' epilogues have read it
     uint64_t gfull[GATHER_BUFS];
@@ -80,8 +105,7 @@ struct AgCtrl {
 };
 
 constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + AG_STAGES * A_STAGE_BYTES;
-constexpr int OFF_EPI = OFF_B + AG_STAGES * B_HALF_BYTES;
+constexpr int OFF_EPI = OFF_A + Shape<1>::RING_END;
 constexpr int OFF_GATHER = OFF_EPI + 4 * EPI_WARP_BYTES;
 constexpr int OFF_CTRL = OFF_GATHER + GATHER_BUFS * GATHER_BUF_BYTES;
 constexpr int SMEM_ALLOC = OFF_CTRL + static_cast<int>(sizeof(AgCtrl)) + 1024;
@@ -92,7 +116,7 @@ static_assert(SMEM_ALLOC <= 232448, "shared memory budget (227 KiB per CTA)");
 constexpr int PROD_WARPS_FIT = OFF_CTRL / (PROD_BUFS * GATHER_BUF_BYTES);
 constexpr int PROD_WARPS = PROD_WARPS_FIT < 8 ? PROD_WARPS_FIT : 8;
 static_assert(PROD_WARPS >= 1, "room for at least one producer warp");
-static_assert(OFF_B % 1024 == 0 && OFF_EPI % 1024 == 0 && OFF_GATHER % 1024 == 0,
+static_assert(OFF_EPI % 1024 == 0 && OFF_GATHER % 1024 == 0,
               "swizzled buffers must be 1024-byte aligned");
 
 // The loader asks for its next tile this many k-blocks before the end of the
@@ -109,7 +133,7 @@ constexpr int CLAIM_LEAD_KB = 64;
 constexpr uint32_t TQ_READERS = 1 + 1 + 4 + 1;
 constexpr uint32_t TQ_ODD_READERS = 1 + 4;
 
-constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators of 256 columns
+constexpr uint32_t TMEM_COLS = 2 * BN;  // two 256-column accumulators, or one of 512
 constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, /*B MN-major*/ true);
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p)
@@ -297,8 +321,9 @@ struct LoaderRing {
 };
 
 // Issue the TMA loads of this CTA's half of k-blocks [kb0, kb1) of a pair
-// tile (A rows from m0, B columns from n0): the plain GEMM pipeline, with
-// nothing else in the loop.
+// tile (A rows from m0; B columns n0 + 256 h .. + 127 for each MMA h of the
+// k step): the plain GEMM pipeline, with nothing else in the loop.
+template <int NW>
 __device__ __forceinline__ bool issue_kblocks(const AgParams& p, uint8_t* smem, AgCtrl* ctrl,
                                               const ErrCtx& ec, LoaderRing& rg,
                                               const CUtensorMap* amap, int m0, int n0,
@@ -309,17 +334,20 @@ __device__ __forceinline__ bool issue_kblocks(const AgParams& p, uint8_t* smem, 
         if (!wait_bar(&ctrl->empty[rg.stage], rg.sphase ^ 1u, ec, SITE_LOADER_EMPTY)) return false;
         if (lane == 0) {
             const uint32_t fb = mapa_shared(smem_u32(&ctrl->full[rg.stage]), 0);
-            if (crank == 0) mbar_arrive_expect_tx(&ctrl->full[rg.stage], PAIR_TX_BYTES);
+            if (crank == 0) mbar_arrive_expect_tx(&ctrl->full[rg.stage], Shape<NW>::TX);
             tma_load_2d_pair(smem + OFF_A + rg.stage * A_STAGE_BYTES, amap, fb, kb * BK, m0);
-            uint8_t* bs = smem + OFF_B + rg.stage * B_HALF_BYTES;
+            uint8_t* bs = smem + Shape<NW>::OFF_B + rg.stage * Shape<NW>::B_STAGE;
 #pragma unroll
-            for (int j = 0; j < HALF_N / 64; ++j)
-                tma_load_2d_pair(bs + j * B_CHUNK_BYTES, &p.b_load, fb, n0 + 64 * j, kb * BK);
+            for (int h = 0; h < NW; ++h)
+#pragma unroll
+                for (int j = 0; j < HALF_N / 64; ++j)
+                    tma_load_2d_pair(bs + h * B_HALF_BYTES + j * B_CHUNK_BYTES, &p.b_load, fb,
+                                     n0 + h * BN + 64 * j, kb * BK);
         }
         __syncwarp();
         rg.filled |= 1u << rg.stage;
         rg.last_par = (rg.last_par & ~(1u << rg.stage)) | (rg.sphase << rg.stage);
-        if (++rg.stage == AG_STAGES) { rg.stage = 0; rg.sphase ^= 1u; }
+        if (++rg.stage == Shape<NW>::STAGES) { rg.stage = 0; rg.sphase ^= 1u; }
     }
     return true;
 }
@@ -452,6 +480,7 @@ __device__ void run_scheduler(const AgParams& p, AgCtrl* ctrl, const ErrCtx& ec)
 
 // Warp 0 of both CTAs: takes tiles from the queue (their flags already
 // acquired) and streams this CTA's half of their k-blocks through the ring.
+template <int NW>
 __device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const ErrCtx& ec,
                            uint32_t crank)
 {
@@ -468,19 +497,19 @@ __device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
         if (lane == 0) fence_async_global();
         __syncwarp();
         const int m0 = (q / p.T_N) * PAIR_M + static_cast<int>(crank) * BM;
-        const int n0 = (q % p.T_N) * BN + static_cast<int>(crank) * HALF_N;
+        const int n0 = (q % p.T_N) * (NW * BN) + static_cast<int>(crank) * HALF_N;
         const bool loc = local_half(p, m0);
         const CUtensorMap* amap = loc ? &p.a_local_load : &p.g_load;
         const int ay = loc ? m0 - p.local_rank * p.M_r : m0;
         const int kb_ask = KB > CLAIM_LEAD_KB ? KB - CLAIM_LEAD_KB : 0;
-        if (!issue_kblocks(p, smem, ctrl, ec, rg, amap, ay, n0, 0, kb_ask, crank)) break;
+        if (!issue_kblocks<NW>(p, smem, ctrl, ec, rg, amap, ay, n0, 0, kb_ask, crank)) break;
         if (crank == 0 && lane == 0) mbar_arrive(&ctrl->need_next);
-        if (!issue_kblocks(p, smem, ctrl, ec, rg, amap, ay, n0, kb_ask, KB, crank)) break;
+        if (!issue_kblocks<NW>(p, smem, ctrl, ec, rg, amap, ay, n0, kb_ask, KB, crank)) break;
     }
     // The even CTA's `full` phases cover both CTAs' loads: every armed one
     // must complete before the pair may exit.
     if (crank == 0)
-        for (int st = 0; st < AG_STAGES; ++st)
+        for (int st = 0; st < Shape<NW>::STAGES; ++st)
             if (rg.filled & (1u << st)) drain_bar(&ctrl->full[st], (rg.last_par >> st) & 1u, ec);
 }
 
@@ -493,6 +522,7 @@ __device__ void run_loader(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, const
 // divisions, and descriptors stepped by addition (the start-address field
 // is the shared address >> 4) kept the k-block at about 515 cycles against
 // 570 for the same loop run by a whole warp.
+template <int NW>
 __device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t tmem,
                         const ErrCtx& ec)
 {
@@ -502,7 +532,7 @@ __device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t
     const uint64_t a_desc0 = sdesc_sw128(smem_u32(smem + OFF_A), 16, 1024);
     // B: N-major, 64-column chunks 8 KiB apart (LBO), 8-row K groups 1024 B
     //    apart (SBO); k steps of 16 rows advance 2 KiB.
-    const uint64_t b_desc0 = sdesc_sw128(smem_u32(smem + OFF_B), B_CHUNK_BYTES, 1024);
+    const uint64_t b_desc0 = sdesc_sw128(smem_u32(smem + Shape<NW>::OFF_B), B_CHUNK_BYTES, 1024);
     uint32_t stage = 0, sphase = 0, acc = 0, aphase = 0, tq = 0, tqphase = 0;
     bool ok = true;
     while (ok) {
@@ -517,17 +547,20 @@ __device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t
             if (!wait_bar(&ctrl->full[stage], sphase, ec, SITE_MMA_FULL)) { ok = false; break; }
             tc_fence_after();
             const uint64_t ad = a_desc0 + stage * (A_STAGE_BYTES >> 4);
-            const uint64_t bd = b_desc0 + stage * (B_HALF_BYTES >> 4);
+            const uint64_t bd = b_desc0 + stage * (Shape<NW>::B_STAGE >> 4);
 #pragma unroll
             for (int k = 0; k < BK / UMMA_K; ++k)
-                mma_bf16_pair(d, ad + k * ((UMMA_K * 2) >> 4), bd + k * ((UMMA_K * 128) >> 4), IDESC,
-                              (kb | k) != 0 ? 1u : 0u);
+#pragma unroll
+                for (int h = 0; h < NW; ++h)  // MMA h: tile columns 256 h .. 256 h + 255
+                    mma_bf16_pair(d + h * BN, ad + k * ((UMMA_K * 2) >> 4),
+                                  bd + h * (B_HALF_BYTES >> 4) + k * ((UMMA_K * 128) >> 4), IDESC,
+                                  (kb | k) != 0 ? 1u : 0u);
             mma_commit_pair(&ctrl->empty[stage], 0x3);  // frees both CTAs' stage when done
-            if (++stage == AG_STAGES) { stage = 0; sphase ^= 1u; }
+            if (++stage == Shape<NW>::STAGES) { stage = 0; sphase ^= 1u; }
         }
         if (!ok) break;
         mma_commit_pair(&ctrl->tmem_full[acc], 0x3);
-        if (++acc == 2) { acc = 0; aphase ^= 1u; }
+        if (++acc == Shape<NW>::ACCS) { acc = 0; aphase ^= 1u; }
     }
     // Every MMA issued must complete before TMEM is released.
     mma_commit_pair(&ctrl->mma_done, 0x1);
@@ -536,7 +569,10 @@ __device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t
 
 // ------------------------------------------------------------------ epilogue
 
-// Warps 4-7 of both CTAs: this CTA's 128 rows of each pair tile.
+// Warps 4-7 of both CTAs: this CTA's 128 rows of each pair tile.  With one
+// accumulator (NW = 2) the MMA waits for the whole read-out before the next
+// tile, so the accumulator is released right after the last TMEM load.
+template <int NW>
 __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t tmem,
                              const ErrCtx& ec, int warp, uint32_t crank)
 {
@@ -552,19 +588,19 @@ __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uin
         if (q < 0) break;
 
         const int m0 = (q / p.T_N) * PAIR_M + static_cast<int>(crank) * BM;
-        const int n0 = (q % p.T_N) * BN;
+        const int n0 = (q % p.T_N) * (NW * BN);
         const int row0 = m0 + quarter * 32;
         if (!wait_bar(&ctrl->tmem_full[acc], aphase, ec, SITE_EPI_TMEM_FULL)) break;
         tc_fence_after();
         const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 64; ++ch) {
+        for (int ch = 0; ch < Shape<NW>::CHUNKS; ++ch) {
             uint32_t v0[32], v1[32];
             tmem_ld32(taddr + ch * 64, v0);
             tmem_ld32(taddr + ch * 64 + 32, v1);
             tmem_ld_wait(v0);
             tmem_ld_wait(v1);
-            if (ch == BN / 64 - 1) {
+            if (ch == Shape<NW>::CHUNKS - 1) {
                 // accumulator fully read: the MMA may reuse it
                 tc_fence_before();
                 __syncwarp();
@@ -593,7 +629,7 @@ __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uin
             }
             __syncwarp();
         }
-        if (++acc == 2) { acc = 0; aphase ^= 1u; }
+        if (++acc == Shape<NW>::ACCS) { acc = 0; aphase ^= 1u; }
     }
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
@@ -833,6 +869,7 @@ __device__ void run_gather(const AgParams& p, uint8_t* buf0, uint64_t* gfull, in
 
 // ------------------------------------------------------------------ kernel
 
+template <int NW>
 __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__ AgParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -844,7 +881,7 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
     const bool producer = p.role != OPW_ROLE_CONSUMER;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < AG_STAGES; ++i) {
+        for (int i = 0; i < Shape<NW>::STAGES; ++i) {
             mbar_init(&ctrl->full[i], 1);
             mbar_init(&ctrl->empty[i], 1);
         }
@@ -898,9 +935,9 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
                        &ctrl->gprod[warp * PROD_BUFS], PROD_BUFS, ec, t_start);
     } else if (!skip) {
         if (warp == 0) {
-            if (consumer) run_loader(p, smem, ctrl, ec, crank);
+            if (consumer) run_loader<NW>(p, smem, ctrl, ec, crank);
         } else if (warp == 1) {
-            if (consumer && crank == 0 && lane_id() == 0) run_mma(p, smem, ctrl, tmem, ec);
+            if (consumer && crank == 0 && lane_id() == 0) run_mma<NW>(p, smem, ctrl, tmem, ec);
         } else if (warp == 2) {
             if (producer)
                 run_gather(p, smem + OFF_GATHER, ctrl->gfull, GATHER_BUFS, ec, t_start);
@@ -908,7 +945,7 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
             if (consumer && crank == 0) run_scheduler(p, ctrl, ec);
             if (consumer && crank == 1) run_forwarder(ctrl, ec);
         } else {
-            if (consumer) run_epilogue(p, smem, ctrl, tmem, ec, warp, crank);
+            if (consumer) run_epilogue<NW>(p, smem, ctrl, tmem, ec, warp, crank);
         }
     }
 
@@ -946,7 +983,9 @@ bool set_smem_attr()
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(ag_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(ag_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_ALLOC) != cudaSuccess ||
+            cudaFuncSetAttribute(ag_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_ALLOC) != cudaSuccess)
             return false;
         attr_set[dev] = true;
@@ -971,8 +1010,12 @@ int ag_max_pairs()
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = pair_config(static_cast<unsigned>(sms / 2), nullptr, attr);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, ag_gemm_kernel, &cfg) != cudaSuccess) return 0;
+    // both widths use the same shared memory, threads and cluster shape
+    int n1 = 0, n2 = 0;
+    if (cudaOccupancyMaxActiveClusters(&n1, ag_gemm_kernel<1>, &cfg) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n2, ag_gemm_kernel<2>, &cfg) != cudaSuccess)
+        return 0;
+    const int n = n1 < n2 ? n1 : n2;
     cached[dev] = n;
     return n;
 }
@@ -982,7 +1025,8 @@ cudaError_t launch_ag_gemm(const AgParams& p, int pairs, cudaStream_t s)
     if (!set_smem_attr()) return cudaErrorInvalidDevice;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = pair_config(static_cast<unsigned>(pairs), s, attr);
-    return cudaLaunchKernelEx(&cfg, ag_gemm_kernel, p);
+    return p.tile_n == 2 * BN ? cudaLaunchKernelEx(&cfg, ag_gemm_kernel<2>, p)
+                              : cudaLaunchKernelEx(&cfg, ag_gemm_kernel<1>, p);
 }
 
 }  // namespace opw

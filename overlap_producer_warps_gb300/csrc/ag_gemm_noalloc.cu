@@ -121,7 +121,9 @@ extern "C" opw_status opw_ag_gemm_noalloc(const opw_symm* symm, size_t a_off, in
     int64_t* flags = static_cast<int64_t*>(scratch);
     unsigned long long* counters = static_cast<unsigned long long*>(scratch) + kMaxFlags;
     AgParams p;
-    const opw_status st_params = ag_fill_params(symm, a_off, M_r, N, K, ft, B_dev, G_dev, C_dev, o, &p);
+    const int tile_n = ag_tile_n_for(o, pairs, static_cast<int64_t>(symm->R) * M_r, N);
+    const opw_status st_params =
+        ag_fill_params(symm, a_off, M_r, N, K, ft, B_dev, G_dev, C_dev, o, tile_n, &p);
     if (st_params != OPW_OK) return st_params;
     p.flags = flags;
     p.status = status_dev;

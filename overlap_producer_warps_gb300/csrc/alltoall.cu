@@ -160,7 +160,7 @@ opw_status opw_alltoall(const opw_symm* symm, size_t send_off, size_t recv_off,
     if (opts != nullptr) o = *opts;
     if (o.sync_mode != 0 || o.schedule != 0 || o.role != 0 || o.publish_perm != nullptr ||
         o.delay_ns != nullptr || o.fault_kind != 0 || o.num_ctas < 0 || o.signal_mode != 0 ||
-        o.local_rank < -1 || o.local_rank > 0 || o.trace_dev != nullptr)
+        o.local_rank < -1 || o.local_rank > 0 || o.trace_dev != nullptr || o.tile_n != 0)
         return OPW_ERR_INVALID_ARG;
     const int R = symm->R;
     if (bytes_per_peer <= 0 || bytes_per_peer % 16 != 0 || bytes_per_peer > (int64_t(1) << 40))

@@ -146,6 +146,7 @@ opw_status ag_check_args(const opw_symm* symm, size_t a_off, int64_t M_r, int64_
     if (o.num_ctas < 0) return OPW_ERR_INVALID_ARG;
     if (o.signal_mode != OPW_SIGNAL_TILE_SET && o.signal_mode != OPW_SIGNAL_ROW_ADD)
         return OPW_ERR_INVALID_ARG;
+    if (o.tile_n != 0 && o.tile_n != BN && o.tile_n != 2 * BN) return OPW_ERR_INVALID_ARG;
     const int R = symm->R;
     if (o.local_rank < -1 || o.local_rank >= R) return OPW_ERR_INVALID_ARG;
     if (o.publish_perm != nullptr) {
@@ -181,9 +182,24 @@ int ag_pairs_for(const opw_opts& o, int dev)
     return pairs < max_pairs ? pairs : max_pairs;
 }
 
+int ag_tile_n_for(const opw_opts& o, int pairs, int64_t M, int64_t N)
+{
+    if (o.tile_n != 0) return o.tile_n;
+    if (pairs <= 0) return BN;
+    // Whole waves of pair tiles: a 256 x 512 tile takes about 1.93 times as
+    // long as a 256 x 256 one (its epilogue is not overlapped), so it pays
+    // only when it needs fewer than that many times the 256-wide waves.  On
+    // the TP layer (512 tiles of 256 x 256 on 76 pairs) 7 waves beat 4 x 1.93;
+    // on the MLP and skew layers (12 and 54 waves) the wide tiles win.
+    const int64_t tm = (M + PAIR_M - 1) / PAIR_M;
+    const int64_t w1 = (tm * ((N + BN - 1) / BN) + pairs - 1) / pairs;
+    const int64_t w2 = (tm * ((N + 2 * BN - 1) / (2 * BN)) + pairs - 1) / pairs;
+    return w2 * 193 < w1 * 100 ? 2 * BN : BN;
+}
+
 opw_status ag_fill_params(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t N, int64_t K,
                           int64_t ft, const void* B_dev, void* G_dev, void* C_dev,
-                          const opw_opts& o, AgParams* pp)
+                          const opw_opts& o, int tile_n, AgParams* pp)
 {
     AgParams& p = *pp;
     std::memset(&p, 0, sizeof p);
@@ -217,7 +233,8 @@ opw_status ag_fill_params(const opw_symm* symm, size_t a_off, int64_t M_r, int64
     p.T_mr = static_cast<int32_t>(M_r / ft);
     p.T_k = static_cast<int32_t>(K / ft);
     p.T_M = static_cast<int32_t>((M + PAIR_M - 1) / PAIR_M);
-    p.T_N = static_cast<int32_t>((N + BN - 1) / BN);
+    p.tile_n = tile_n;
+    p.T_N = static_cast<int32_t>((N + tile_n - 1) / tile_n);
     p.role = o.role;
     p.sync_mode = o.sync_mode;
     p.schedule = o.schedule;
@@ -389,6 +406,19 @@ int64_t opw_ag_trace_words(int32_t R, int64_t M_r, int64_t N, int64_t K)
     return 2 * F + 2 * T + OPW_TRACE_MAX_CTAS;
 }
 
+int32_t opw_ag_tile_n(int32_t R, int64_t M_r, int64_t N, const opw_opts* opts_in)
+{
+    opw_opts tmp;
+    const opw_opts& o = opts_or_default(opts_in, tmp);
+    if (R < 1 || R > OPW_MAX_RANKS || M_r <= 0 || N <= 0 || o.num_ctas < 0) return -1;
+    if (o.tile_n != 0) return (o.tile_n == BN || o.tile_n == 2 * BN) ? o.tile_n : -1;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    const int pairs = opw::ag_pairs_for(o, dev);
+    if (pairs <= 0) return -1;
+    return opw::ag_tile_n_for(o, pairs, static_cast<int64_t>(R) * M_r, N);
+}
+
 opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t N, int64_t K,
                        const void* B_dev, void* G_dev, void* C_dev, opw_signal* sig,
                        uint64_t epoch, const opw_opts* opts_in, void* stream)
@@ -418,7 +448,8 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
     const int pairs = opw::ag_pairs_for(o, dev);
     if (pairs <= 0) return OPW_ERR_CUDA;
     AgParams p;
-    st = opw::ag_fill_params(symm, a_off, M_r, N, K, ft, B_dev, G_dev, C_dev, o, &p);
+    const int tile_n = opw::ag_tile_n_for(o, pairs, static_cast<int64_t>(R) * M_r, N);
+    st = opw::ag_fill_params(symm, a_off, M_r, N, K, ft, B_dev, G_dev, C_dev, o, tile_n, &p);
     if (st != OPW_OK) return st;
     p.flags = sig->flags;
     p.status = sig->status;
@@ -477,7 +508,8 @@ opw_status gemm_rs_launch(const opw_symm* symm, size_t a_off, size_t b_off, size
     if ((o.sync_mode != OPW_SYNC_OVERLAP && o.sync_mode != OPW_SYNC_CHECKED) || o.schedule != 0 ||
         o.role < OPW_ROLE_FUSED || o.role > OPW_ROLE_CONSUMER || o.publish_perm != nullptr ||
         o.delay_ns != nullptr || (o.fault_kind != OPW_FAULT_NONE && o.fault_kind != OPW_FAULT_DROP_TILE) ||
-        o.num_ctas < 0 || o.signal_mode != 0 || o.local_rank < -1 || o.local_rank > 0)
+        o.num_ctas < 0 || o.signal_mode != 0 || o.local_rank < -1 || o.local_rank > 0 ||
+        o.tile_n != 0)
         return OPW_ERR_INVALID_ARG;
     // the receiving side waits on published tiles: only a fused launch publishes results
     if (recv_dev != nullptr && o.role != OPW_ROLE_FUSED) return OPW_ERR_INVALID_ARG;

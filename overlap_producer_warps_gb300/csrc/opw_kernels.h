@@ -68,7 +68,8 @@ struct AgParams {
     int32_t R, M_r, M, N, K;
     int32_t ft;               // flag tile edge (64 or 128)
     int32_t T_mr, T_k;        // flag tiles per rank along M, along K
-    int32_t T_M, T_N;         // PAIR_M x BN pair tiles along M, along N
+    int32_t T_M, T_N;         // PAIR_M x tile_n pair tiles along M, along N
+    int32_t tile_n;           // pair tile columns: BN or 2 * BN (host's choice per launch)
     int32_t role, sync_mode, schedule;
     int32_t group_rows;       // both schedules: pair rows per rasterisation group
     int32_t tpr;              // pair rows per rank (M_r / 256), 0 when a rank's rows are
@@ -134,11 +135,13 @@ opw_status ag_check_args(const opw_symm* symm, size_t a_off, int64_t M_r, int64_
                          const opw_opts& o, int64_t* ft);
 // CTA pairs to launch for these options on device `dev` (0 on error).
 int ag_pairs_for(const opw_opts& o, int dev);
+// Pair tile columns (BN or 2 * BN) for a launch of `pairs` pairs on an M x N output.
+int ag_tile_n_for(const opw_opts& o, int pairs, int64_t M, int64_t N);
 // Tensor maps, shapes and options of the launch; the caller sets flags,
 // status, counters, epoch, claim_base and rank_target.
 opw_status ag_fill_params(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t N, int64_t K,
                           int64_t ft, const void* B_dev, void* G_dev, void* C_dev,
-                          const opw_opts& o, AgParams* p);
+                          const opw_opts& o, int tile_n, AgParams* p);
 cudaError_t launch_ag_gemm(const AgParams& p, int pairs, cudaStream_t s);
 int rs_max_pairs();  // clusters of 2 GEMM-RS CTAs that fit at once (0 on error)
 cudaError_t launch_gemm_rs(const RsParams& p, int pairs, cudaStream_t s);

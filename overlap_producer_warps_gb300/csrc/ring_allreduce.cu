@@ -226,7 +226,7 @@ opw_status opw_ring_allreduce(const opw_symm* symm, size_t data_off, size_t recv
     if (opts != nullptr) o = *opts;
     if (o.sync_mode != 0 || o.schedule != 0 || o.role != 0 || o.publish_perm != nullptr ||
         o.delay_ns != nullptr || o.fault_kind != 0 || o.num_ctas < 0 || o.signal_mode != 0 ||
-        o.local_rank < -1 || o.local_rank > 0 || o.trace_dev != nullptr)
+        o.local_rank < -1 || o.local_rank > 0 || o.trace_dev != nullptr || o.tile_n != 0)
         return OPW_ERR_INVALID_ARG;
     const int R = symm->R;
     if (n <= 0 || n % (4 * R) != 0 || n / R > (int64_t(1) << 40)) return OPW_ERR_UNSUPPORTED_SHAPE;

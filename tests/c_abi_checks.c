@@ -34,7 +34,7 @@ int main(void)
     symm.rank_off = rank_off;
     symm.R = 2;
 
-    EXPECT(opw_abi_version() == 1);
+    EXPECT(opw_abi_version() == 2);
     EXPECT(strcmp(opw_status_str(OPW_OK), "OK") == 0);
     EXPECT(strcmp(opw_status_str(OPW_ERR_FLAG_PROTOCOL), "FLAG_PROTOCOL") == 0);
 
@@ -50,7 +50,15 @@ int main(void)
     /* options default */
     opw_opts o;
     opw_opts_default(&o);
-    EXPECT(o.sync_mode == OPW_SYNC_OVERLAP && o.role == OPW_ROLE_FUSED && o.local_rank == 0);
+    EXPECT(o.sync_mode == OPW_SYNC_OVERLAP && o.role == OPW_ROLE_FUSED && o.local_rank == 0 &&
+           o.tile_n == 0);
+    /* pair tile width: an explicit choice is returned as is; others are refused */
+    opw_opts wide = o;
+    wide.tile_n = 512;
+    EXPECT(opw_ag_tile_n(2, 128, 1024, &wide) == 512);
+    wide.tile_n = 384;
+    EXPECT(opw_ag_tile_n(2, 128, 1024, &wide) == -1);
+    EXPECT(opw_ag_tile_n(0, 128, 1024, NULL) == -1);
 
     /* AG-GEMM argument checks, through the entry that needs no signal object */
     EXPECT(opw_ag_gemm_noalloc(&symm, 0, 128, 256, 256, B, G, C, NULL, NULL, NULL) ==
@@ -69,6 +77,10 @@ int main(void)
            OPW_ERR_MISALIGNED);                                    /* status word */
     opw_opts bad = o;
     bad.local_rank = 2; /* R = 2 */
+    EXPECT(opw_ag_gemm_noalloc(&symm, 0, 128, 256, 256, B, G, C, status, &bad, NULL) ==
+           OPW_ERR_INVALID_ARG);
+    bad = o;
+    bad.tile_n = 128; /* pair tiles are 256 or 512 wide */
     EXPECT(opw_ag_gemm_noalloc(&symm, 0, 128, 256, 256, B, G, C, status, &bad, NULL) ==
            OPW_ERR_INVALID_ARG);
     bad = o;

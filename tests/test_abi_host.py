@@ -50,11 +50,12 @@ def test_struct_layout_matches_c_compiler(api):
 #include <stdio.h>
 #include "opw.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(opw_opts),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(opw_opts),
     offsetof(opw_opts, timeout_ns), offsetof(opw_opts, sync_mode), offsetof(opw_opts, schedule),
     offsetof(opw_opts, role), offsetof(opw_opts, num_ctas), offsetof(opw_opts, publish_perm),
     offsetof(opw_opts, delay_ns), offsetof(opw_opts, trace_dev), offsetof(opw_opts, fault_kind),
-    offsetof(opw_opts, fault_arg), offsetof(opw_opts, signal_mode), offsetof(opw_opts, local_rank));
+    offsetof(opw_opts, fault_arg), offsetof(opw_opts, signal_mode), offsetof(opw_opts, local_rank),
+    offsetof(opw_opts, tile_n));
   printf("%zu %zu %zu %zu %zu\n", sizeof(opw_symm), offsetof(opw_symm, heap_dev),
     offsetof(opw_symm, rank_off), offsetof(opw_symm, R), offsetof(opw_symm, reserved));
   return 0;
@@ -89,7 +90,7 @@ def test_status_strings(api):
                        (4, "BAD_EPOCH"), (5, "CUDA_ERROR"), (6, "TIMEOUT"), (7, "FLAG_PROTOCOL"),
                        (8, "NOT_READY"), (99, "UNKNOWN")]:
         assert api.status_str(code) == name
-    assert api.lib().opw_abi_version() == 1
+    assert api.lib().opw_abi_version() == 2
 
 
 def test_flag_geometry(api):
@@ -168,6 +169,13 @@ def test_ag_gemm_rejects_bad_arguments_on_the_host(api):
     assert _ag(api, opts=api.make_opts(signal_mode=2)) == E.ERR_INVALID_ARG
     assert _ag(api, opts=api.make_opts(local_rank=-2)) == E.ERR_INVALID_ARG
     assert _ag(api, opts=api.make_opts(local_rank=2)) == E.ERR_INVALID_ARG   # R = 2
+    for tn in (128, 384, 1024, -256):                   # pair tiles are 256 or 512 wide
+        assert _ag(api, opts=api.make_opts(tile_n=tn)) == E.ERR_INVALID_ARG
+    # an explicit tile width is returned as is, without a device
+    assert api.ag_tile_n(2, 128, 1024, api.make_opts(tile_n=512)) == 512
+    assert api.ag_tile_n(2, 128, 1024, api.make_opts(tile_n=256)) == 256
+    assert api.ag_tile_n(2, 128, 1024, api.make_opts(tile_n=384)) == -1
+    assert api.ag_tile_n(9, 128, 1024, api.make_opts(tile_n=256)) == -1
     # a signal object with too few slots (here: none)
     assert _ag(api) == E.ERR_INVALID_ARG
 
@@ -188,6 +196,7 @@ def test_gemm_rs_rejects_bad_arguments_on_the_host(api):
     assert rs(opts=api.make_opts(publish_perm=[1, 0])) == E.ERR_INVALID_ARG
     assert rs(opts=api.make_opts(role=3)) == E.ERR_INVALID_ARG
     assert rs(opts=api.make_opts(role=-1)) == E.ERR_INVALID_ARG
+    assert rs(opts=api.make_opts(tile_n=512)) == E.ERR_INVALID_ARG   # AG-GEMM only
     assert rs(opts=api.make_opts(sync_mode=api.SYNC_SERIAL)) == E.ERR_INVALID_ARG
     assert rs(opts=api.make_opts(fault_kind=api.FAULT_STALE_EPOCH)) == E.ERR_INVALID_ARG
     assert rs() == E.ERR_INVALID_ARG                    # too few slots

@@ -117,6 +117,56 @@ def test_shapes(api, R, M_r, K, N, order):
     _run_and_check(api, d)
 
 
+@pytest.mark.parametrize("R,M_r,K,N", [
+    (2, 256, 256, 512),     # one 512-wide tile column
+    (4, 256, 512, 776),     # ragged N: the second wide column holds 264 columns
+    (3, 64, 192, 200),      # flag tile 64, N narrower than one wide tile
+    (5, 192, 320, 1032),    # ragged M (960 rows) and N (3 wide columns)
+    (8, 128, 1024, 1024),   # eight ranks, several k-blocks per flag
+])
+def test_wide_pair_tiles_match_oracle_and_narrow_tiles(api, R, M_r, K, N):
+    """256 x 512 pair tiles (two N = 256 MMAs per k step into one 512-column
+    accumulator) against the oracle, and bit for bit against 256 x 256 tiles:
+    every output element sums the same products in the same order."""
+    d = inputs.ag_inputs(_cfg(R, M_r, K, N), seed=R * 11 + N)
+    wide = _run_and_check(api, d, epoch_runs=2, opts_fn=lambda i: api.make_opts(tile_n=512))
+    narrow = _run_and_check(api, d, full=False, opts_fn=lambda i: api.make_opts(tile_n=256))
+    assert np.array_equal(host_bits(wide.G), host_bits(narrow.G))
+    assert np.array_equal(host_bits(wide.C), host_bits(narrow.C))
+
+
+def test_wide_tiles_many_per_pair(api):
+    """Two CTA pairs take 16 wide tiles each, so the one TMEM accumulator is
+    handed between MMA and epilogue many times per launch, over 3 epochs."""
+    d = inputs.ag_inputs(_cfg(4, 512, 512, 2048), seed=77)
+    p1 = _run_and_check(api, d, epoch_runs=3,
+                        opts_fn=lambda i: api.make_opts(tile_n=512, num_ctas=4))
+    p2 = _run_and_check(api, d, full=False,
+                        opts_fn=lambda i: api.make_opts(tile_n=512, num_ctas=4,
+                                                        schedule=api.SCHED_SWIZZLE))
+    assert np.array_equal(host_bits(p1.C), host_bits(p2.C))
+
+
+def test_tile_width_choice(api):
+    """The library's width for the benchmark layers on the full grid follows
+    its documented rule: 512 when whole waves of wide tiles, at 1.93 times a
+    256-wide wave, take less time than the 256-wide waves."""
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    for name in ("ag_tp", "ag_mlp", "ag_skew"):
+        c = inputs.CONFIGS[name]
+        M, N = c["R"] * c["M_r"], c["N"]
+        tm = (M + 255) // 256
+        w1 = -(-tm * (-(-N // 256)) // pairs)
+        w2 = -(-tm * (-(-N // 512)) // pairs)
+        want = 512 if w2 * 193 < w1 * 100 else 256
+        assert api.ag_tile_n(c["R"], c["M_r"], N) == want, name
+        assert api.ag_tile_n(c["R"], c["M_r"], N, api.make_opts(tile_n=256)) == 256
+    if pairs == 76:   # a full GB300: TP stays 256 wide, MLP and skew go wide
+        assert [api.ag_tile_n(inputs.CONFIGS[n]["R"], inputs.CONFIGS[n]["M_r"],
+                              inputs.CONFIGS[n]["N"]) for n in ("ag_tp", "ag_mlp", "ag_skew")] == \
+            [256, 512, 512]
+
+
 def test_epochs_reused_without_reset(api):
     """20 launches on one signal object: flags == e after each (TP-style epochs 1..20)."""
     d = inputs.ag_inputs(_cfg(4, 128, 256, 512), seed=9)
@@ -199,17 +249,19 @@ def test_local_rank_choice_does_not_change_results(api, R, M_r, K, N):
         assert np.array_equal(G, outs[0][0]) and np.array_equal(C, outs[0][1])
 
 
-def _trace_views(api, prob, trace, grid):
+def _trace_views(api, prob, trace, grid, tile_n):
     F = api.ag_num_flags(prob.R, prob.M_r, prob.K)
-    T = ((prob.M + 255) // 256) * ((prob.N + 255) // 256)  # 256x256 pair tiles
+    T = ((prob.M + 255) // 256) * ((prob.N + tile_n - 1) // tile_n)  # 256 x tile_n pair tiles
     t = trace.cpu().numpy().view(np.uint64)
     return dict(publish=t[:F], consume=t[F:2 * F], tile=t[2 * F:2 * F + T],
                 tile_start=t[2 * F + T:2 * F + 2 * T], cta_start=t[2 * F + 2 * T:2 * F + 2 * T + grid],
                 F=F, T=T)
 
 
-@pytest.mark.parametrize("local,perm", [(2, None), (0, None), (1, (3, 0, 2, 1))])
-def test_trace_publish_before_consume_and_swizzle_order(api, local, perm):
+@pytest.mark.parametrize("local,perm,tile_n", [(2, None, 256), (0, None, 256),
+                                               (1, (3, 0, 2, 1), 256), (2, None, 512),
+                                               (1, (3, 0, 2, 1), 512)])
+def test_trace_publish_before_consume_and_swizzle_order(api, local, perm, tile_n):
     R, M_r, K, N = 4, 256, 512, 1024
     d = inputs.ag_inputs(_cfg(R, M_r, K, N), seed=14)
     prob = AgProblem(d)
@@ -217,11 +269,12 @@ def test_trace_publish_before_consume_and_swizzle_order(api, local, perm):
     words = api.ag_trace_words(R, M_r, N, K)
     trace = torch.full((words,), -1, dtype=torch.int64, device="cuda")
     grid = 6
-    prob.run(api, sig, sig.next_epoch(), api.make_opts(trace=trace, num_ctas=grid, local_rank=local,
-                                                       publish_perm=perm,
-                                                       schedule=api.SCHED_SWIZZLE))
+    opts = api.make_opts(trace=trace, num_ctas=grid, local_rank=local, publish_perm=perm,
+                         schedule=api.SCHED_SWIZZLE, tile_n=tile_n)
+    assert api.ag_tile_n(R, M_r, N, opts) == tile_n
+    prob.run(api, sig, sig.next_epoch(), opts)
     assert sig.status()[0] == api.OK
-    v = _trace_views(api, prob, trace, grid)
+    v = _trace_views(api, prob, trace, grid, tile_n)
     # every tile published; every tile of another rank acquired no earlier than
     # its publish; the local rank's own tiles (read in place) never acquired
     per_rank = v["F"] // R
@@ -230,10 +283,11 @@ def test_trace_publish_before_consume_and_swizzle_order(api, local, perm):
     assert np.all(v["consume"][remote] != np.uint64(2 ** 64 - 1))
     assert np.all(v["publish"][remote] <= v["consume"][remote])
     assert np.all(v["consume"][~remote] == np.uint64(2 ** 64 - 1))
-    # each consumer (a CTA pair) visited its 256x256 tiles in the oracle's
-    # order: the page's rotation by the PE's rank (tiles_per_pe = M_r/256 = 1),
-    # or, with a publish order, the own rank first and then the others in it
-    T_M, T_N, pairs = prob.M // 256, (N + 255) // 256, grid // 2
+    # each consumer (a CTA pair) visited its 256 x tile_n tiles in the
+    # oracle's order: the page's rotation by the PE's rank (tiles_per_pe =
+    # M_r/256 = 1), or, with a publish order, the own rank first and then the
+    # others in it
+    T_M, T_N, pairs = prob.M // 256, (N + tile_n - 1) // tile_n, grid // 2
     visit = None if perm is None else [local] + [r for r in perm if r != local]
     pair = (v["tile"] >> np.uint64(32)).astype(np.int64)
     pos = (v["tile"] & np.uint64(0xFFFFFFFF)).astype(np.int64)
@@ -260,12 +314,14 @@ def test_skewed_readiness_order_and_delays(api):
     sig = api.Signal(api.ag_num_flags(R, M_r, K))
     words = api.ag_trace_words(R, M_r, N, K)
     trace = torch.full((words,), -1, dtype=torch.int64, device="cuda")
+    opts = api.make_opts(publish_perm=perm, delay_ns=delay, trace=trace)
+    tile_n = api.ag_tile_n(R, M_r, N, opts)
     for _ in range(2):
         trace.fill_(-1)
-        prob.run(api, sig, sig.next_epoch(),
-                 api.make_opts(publish_perm=perm, delay_ns=delay, trace=trace))
+        prob.run(api, sig, sig.next_epoch(), opts)
         assert sig.status()[0] == api.OK
-        v = _trace_views(api, prob, trace, torch.cuda.get_device_properties(0).multi_processor_count)
+        v = _trace_views(api, prob, trace, torch.cuda.get_device_properties(0).multi_processor_count,
+                         tile_n)
         per_rank = v["F"] // R
         pub = v["publish"].reshape(R, per_rank)
         for i in range(1, R):
@@ -362,7 +418,8 @@ def test_launch_behind_another_streams_gemm(api, perm):
         for _ in range(4):
             torch.matmul(big, big, out=out)
     e = sig.next_epoch()
-    prob.run(api, sig, e, api.make_opts(trace=trace, publish_perm=perm))
+    opts = api.make_opts(trace=trace, publish_perm=perm)
+    prob.run(api, sig, e, opts)
     torch.cuda.synchronize()
     assert sig.status()[0] == api.OK
     assert np.all(sig.flags().cpu().numpy() == e)
@@ -370,5 +427,6 @@ def test_launch_behind_another_streams_gemm(api, perm):
     assert np.array_equal(host_bits(prob.G), G_ref)
     assert_gemm_close(host_bits(prob.C), C_ref)
     grid = torch.cuda.get_device_properties(0).multi_processor_count
-    starts = _trace_views(api, prob, trace, grid)["cta_start"].astype(np.float64)
+    starts = _trace_views(api, prob, trace, grid, api.ag_tile_n(R, M_r, N, opts))["cta_start"]
+    starts = starts.astype(np.float64)
     print(f"CTA start spread: {(starts.max() - starts.min()) / 1e3:.1f} us")
