@@ -63,28 +63,32 @@ constexpr int B_HALF_BYTES = BK * HALF_N * 2;   // 16 KiB: 2 chunks of 64 column
 //           buffers it fits the budget (225 KiB); against 5 stages with 4
 //           buffers it was 1.3-2.2 % faster fused in a burst.
 //   NW = 2: two N = 256 MMAs per k step (B columns 0-255 and 256-511 of the
-//           tile) into one 512-column accumulator; a 4-stage ring of 48 KiB
-//           stages (4 x 1024 cycles of MMA in flight).  A CTA reads a quarter
-//           less operand data from L2 per FLOP; the epilogue no longer overlaps
-//           the next tile's MMAs.  In a probe GEMM with this epilogue, random
-//           operands and whole waves it ran 3.7 % faster in a burst and 5-8 %
-//           faster under the power cap, where the lower on-chip traffic bought
-//           a 9 % higher SM clock.
+//           tile) into one 512-column accumulator; a 3-stage ring of 48 KiB
+//           stages (3 x 1024 cycles of MMA in flight, as much as the 6 narrow
+//           stages) and 4 staging buffers per epilogue warp, since the MMA
+//           waits for the whole read-out of the accumulator.  A CTA reads a
+//           quarter less operand data from L2 per FLOP.  In a probe GEMM with
+//           random operands and whole waves it ran 3.7 % faster in a burst and
+//           5-8 % faster under the power cap, where the lower on-chip traffic
+//           bought a 9 % higher SM clock.
 // The host picks the width per launch (opts.tile_n, or from the wave counts).
 template <int NW>
 struct Shape {
-    static constexpr int STAGES = NW == 1 ? 6 : 4;
+    static constexpr int STAGES = NW == 1 ? 6 : 3;
     static constexpr int B_STAGE = NW * B_HALF_BYTES;   // this CTA's B bytes per stage
     static constexpr int OFF_B = STAGES * A_STAGE_BYTES;
-    static constexpr int RING_END = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;  // the ring ends here
+    static constexpr int EPI_BUFS = NW == 1 ? 1 : 4;    // staging buffers per epilogue warp
+    static constexpr int EPI_END = OFF_EPI + 4 * EPI_BUFS * EPI_WARP_BYTES;
     static constexpr uint32_t TX = 2u * (A_STAGE_BYTES + B_STAGE);  // both CTAs' bytes per stage
     static constexpr int ACCS = NW == 1 ? 2 : 1;        // TMEM accumulators
     static constexpr int CHUNKS = NW * BN / 64;         // 64-column epilogue chunks per tile
 };
-static_assert(Shape<1>::RING_END == Shape<2>::RING_END, "both rings fill the same space");
+static_assert(Shape<1>::EPI_END == Shape<2>::EPI_END, "both layouts end where the gather starts");
 static_assert(Shape<1>::OFF_B % 1024 == 0 && Shape<2>::OFF_B % 1024 == 0 &&
+                  Shape<1>::OFF_EPI % 1024 == 0 && Shape<2>::OFF_EPI % 1024 == 0 &&
                   A_STAGE_BYTES % 1024 == 0 && B_HALF_BYTES % 1024 == 0,
-              "swizzled stages must be 1024-byte aligned");
+              "swizzled stages and staging buffers must be 1024-byte aligned");
 constexpr int AG_STAGES_MAX = 6;
 
 struct AgCtrl {
@@ -105,8 +109,7 @@ struct AgCtrl {
 };
 
 constexpr int OFF_A = 0;
-constexpr int OFF_EPI = OFF_A + Shape<1>::RING_END;
-constexpr int OFF_GATHER = OFF_EPI + 4 * EPI_WARP_BYTES;
+constexpr int OFF_GATHER = OFF_A + Shape<1>::EPI_END;
 constexpr int OFF_CTRL = OFF_GATHER + GATHER_BUFS * GATHER_BUF_BYTES;
 constexpr int SMEM_ALLOC = OFF_CTRL + static_cast<int>(sizeof(AgCtrl)) + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget (227 KiB per CTA)");
@@ -116,8 +119,7 @@ static_assert(SMEM_ALLOC <= 232448, "shared memory budget (227 KiB per CTA)");
 constexpr int PROD_WARPS_FIT = OFF_CTRL / (PROD_BUFS * GATHER_BUF_BYTES);
 constexpr int PROD_WARPS = PROD_WARPS_FIT < 8 ? PROD_WARPS_FIT : 8;
 static_assert(PROD_WARPS >= 1, "room for at least one producer warp");
-static_assert(OFF_EPI % 1024 == 0 && OFF_GATHER % 1024 == 0,
-              "swizzled buffers must be 1024-byte aligned");
+static_assert(OFF_GATHER % 1024 == 0, "swizzled buffers must be 1024-byte aligned");
 
 // The loader asks for its next tile this many k-blocks before the end of the
 // current one: late enough that a pair never holds more than one tile it has
@@ -569,20 +571,24 @@ __device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t
 
 // ------------------------------------------------------------------ epilogue
 
-// Warps 4-7 of both CTAs: this CTA's 128 rows of each pair tile.  With one
-// accumulator (NW = 2) the MMA waits for the whole read-out before the next
-// tile, so the accumulator is released right after the last TMEM load.
+// Warps 4-7 of both CTAs: this CTA's 128 rows of each pair tile.  Each
+// 64-column chunk goes TMEM -> registers -> bf16 -> swizzled staging rows ->
+// TMA store, with the next chunk's TMEM load in flight meanwhile and up to
+// EPI_BUFS stores still reading their staging buffers (chunks outside C are
+// read from TMEM and dropped).  With one accumulator
+// (NW = 2) the MMA waits for the whole read-out before the next tile, so the
+// accumulator is released as soon as its last chunk is in registers.
 template <int NW>
 __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t tmem,
                              const ErrCtx& ec, int warp, uint32_t crank)
 {
+    using S = Shape<NW>;
     const uint32_t lane = lane_id();
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
-    uint8_t* buf = smem + OFF_EPI + quarter * EPI_WARP_BYTES;
-    const uint32_t row_addr = smem_u32(buf) + lane * 128u;
+    uint8_t* buf0 = smem + S::OFF_EPI + quarter * S::EPI_BUFS * EPI_WARP_BYTES;
     // the even CTA's tmem_empty[0], [1] (adjacent 8-byte barriers)
     const uint32_t empty_caddr0 = mapa_shared(smem_u32(&ctrl->tmem_empty[0]), 0);
-    uint32_t acc = 0, aphase = 0, tq = 0, tqphase = 0;
+    uint32_t acc = 0, aphase = 0, tq = 0, tqphase = 0, nstore = 0;
     while (true) {
         const int q = pop_tile(ctrl, ec, tq, tqphase, crank);
         if (q < 0) break;
@@ -593,43 +599,63 @@ __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uin
         if (!wait_bar(&ctrl->tmem_full[acc], aphase, ec, SITE_EPI_TMEM_FULL)) break;
         tc_fence_after();
         const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-#pragma unroll 1
-        for (int ch = 0; ch < Shape<NW>::CHUNKS; ++ch) {
-            uint32_t v0[32], v1[32];
-            tmem_ld32(taddr + ch * 64, v0);
-            tmem_ld32(taddr + ch * 64 + 32, v1);
-            tmem_ld_wait(v0);
-            tmem_ld_wait(v1);
-            if (ch == Shape<NW>::CHUNKS - 1) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(taddr, v0);
+        tmem_ld32(taddr + 32, v1);
+        tmem_ld_wait(v0);
+        tmem_ld_wait(v1);
+#pragma unroll
+        for (int ch = 0; ch < S::CHUNKS; ++ch) {
+            uint32_t n0v[32], n1v[32];
+            if (ch + 1 < S::CHUNKS) {
+                tmem_ld32(taddr + (ch + 1) * 64, n0v);
+                tmem_ld32(taddr + (ch + 1) * 64 + 32, n1v);
+            } else {
                 // accumulator fully read: the MMA may reuse it
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_caddr0 + 8u * acc);
             }
-            uint32_t w[32];
+            if (row0 < p.M && n0 + ch * 64 < p.N) {  // the same for the whole warp
+                uint32_t w[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                w[i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
-                w[16 + i] = pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
-            }
-            // the previous TMA store must have finished reading the staging rows
-            if (lane == 0) bulk_wait_read<0>();
-            __syncwarp();
-            // row `lane`, 16-byte chunk j stored at chunk j ^ (row & 7): the
-            // 128-byte swizzle the C tensor map expects
+                for (int i = 0; i < 16; ++i) {
+                    w[i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
+                    w[16 + i] = pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
+                }
+                // Stores take the staging buffers in turn, one bulk group
+                // each: the store that last used this buffer is EPI_BUFS
+                // groups back and must have finished reading it.
+                uint8_t* buf = buf0 + (nstore % S::EPI_BUFS) * EPI_WARP_BYTES;
+                ++nstore;
+                const uint32_t row_addr = smem_u32(buf) + lane * 128u;
+                if (lane == 0) bulk_wait_read<S::EPI_BUFS - 1>();
+                __syncwarp();
+                // row `lane`, 16-byte chunk j stored at chunk j ^ (row & 7): the
+                // 128-byte swizzle the C tensor map expects
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), w[4 * j],
-                             w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-            fence_async_shared();
-            __syncwarp();
-            if (lane == 0 && row0 < p.M && n0 + ch * 64 < p.N) {
-                tma_store_2d(&p.c_store, buf, n0 + ch * 64, row0);
-                bulk_commit();
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
+                                 w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&p.c_store, buf, n0 + ch * 64, row0);
+                    bulk_commit();
+                }
+                __syncwarp();
             }
-            __syncwarp();
+            if (ch + 1 < S::CHUNKS) {
+                tmem_ld_wait(n0v);
+                tmem_ld_wait(n1v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    v0[i] = n0v[i];
+                    v1[i] = n1v[i];
+                }
+            }
         }
-        if (++acc == Shape<NW>::ACCS) { acc = 0; aphase ^= 1u; }
+        if (++acc == S::ACCS) { acc = 0; aphase ^= 1u; }
     }
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
