@@ -594,6 +594,7 @@ def ag_config_results(api, torch, name, peak_tflops, reps):
     e = (med["producer_only"] + med["consumer_only"] - med["fused"]) / min(
         med["producer_only"], med["consumer_only"])
     out = {
+        "pair_tile": f"256x{api.ag_tile_n(R, M_r, N)}",
         "fused_tflops": fl / med["fused"] / 1e9,
         "fused_tflops_best": fl / t["fused"]["min"] / 1e9,
         "pct_of_peak": fl / med["fused"] / 1e9 / peak_tflops,
@@ -861,6 +862,7 @@ def run_ours(args, rank, world, dist):
             "impl": "ours",
             "config": {"workload": WORKLOAD, "R": d["R"], "M_r": d["M_r"], "K": d["K"],
                        "N": d["N"], "schedule": "ready (default)",
+                       "pair_tile": f"256x{api.ag_tile_n(d['R'], d['M_r'], d['N'])}",
                        "publish_perm": None if perm is None else [int(v) for v in perm],
                        "delay_us": None if delay is None else [int(v) // 1000 for v in delay],
                        "epochs": "fresh epoch per launch, no reset",

@@ -10,7 +10,8 @@
 // CTAs work in pairs (clusters of 2) on 256 x 256 output tiles with one
 // tcgen05 cta_group::2 MMA: CTA c of the pair holds rows 128c..128c+127 of
 // the tile's A rows and columns 128c..128c+127 of B in its shared memory and
-// receives its 128 accumulator rows in its own TMEM.  8 warps per CTA:
+// receives its 128 accumulator rows in its own TMEM.  8 warps per CTA (12
+// with 256 x 512 pair tiles):
 //   warp 0     loader (both CTAs): takes tiles from the on-chip tile queue and
 //              TMA-loads this CTA's half of their A k-blocks (from the gathered
 //              buffer G, or in place from the local rank's own shard) and B
@@ -35,7 +36,8 @@
 // shard is local, so its tiles are taken first and its own flags are never
 // waited for; its producer copies still fill G, after every other rank's.
 //   warps 4-7  epilogue (both CTAs): tcgen05.ld -> bf16 (round to nearest
-//              even) -> swizzled shared memory -> TMA store of C.
+//              even) -> swizzled shared memory -> TMA store of C; with
+//              256 x 512 pair tiles warps 8-11 take the second column half.
 // With the gather alone (OPW_ROLE_PRODUCER) there are no consumer roles:
 // warps 0-6 of every CTA are producers, each with staging buffers of its own
 // in the shared memory the ring and the epilogue would use.
@@ -65,8 +67,9 @@ constexpr int B_HALF_BYTES = BK * HALF_N * 2;   // 16 KiB: 2 chunks of 64 column
 //   NW = 2: two N = 256 MMAs per k step (B columns 0-255 and 256-511 of the
 //           tile) into one 512-column accumulator; a 3-stage ring of 48 KiB
 //           stages (3 x 1024 cycles of MMA in flight, as much as the 6 narrow
-//           stages) and 4 staging buffers per epilogue warp, since the MMA
-//           waits for the whole read-out of the accumulator.  A CTA reads a
+//           stages).  The MMA waits for the whole read-out of the accumulator,
+//           so 8 epilogue warps (384 threads) drain its two column halves at
+//           once, each through 2 staging buffers.  A CTA reads a
 //           quarter less operand data from L2 per FLOP.  In a probe GEMM with
 //           random operands and whole waves it ran 3.7 % faster in a burst and
 //           5-8 % faster under the power cap, where the lower on-chip traffic
@@ -78,8 +81,10 @@ struct Shape {
     static constexpr int B_STAGE = NW * B_HALF_BYTES;   // this CTA's B bytes per stage
     static constexpr int OFF_B = STAGES * A_STAGE_BYTES;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;  // the ring ends here
-    static constexpr int EPI_BUFS = NW == 1 ? 1 : 4;    // staging buffers per epilogue warp
-    static constexpr int EPI_END = OFF_EPI + 4 * EPI_BUFS * EPI_WARP_BYTES;
+    static constexpr int EPI_WARPS = 4 * NW;             // warps 4 .. 4 + EPI_WARPS - 1
+    static constexpr int THREADS = 32 * (4 + EPI_WARPS);
+    static constexpr int EPI_BUFS = NW == 1 ? 1 : 2;    // staging buffers per epilogue warp
+    static constexpr int EPI_END = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_WARP_BYTES;
     static constexpr uint32_t TX = 2u * (A_STAGE_BYTES + B_STAGE);  // both CTAs' bytes per stage
     static constexpr int ACCS = NW == 1 ? 2 : 1;        // TMEM accumulators
     static constexpr int CHUNKS = NW * BN / 64;         // 64-column epilogue chunks per tile
@@ -132,8 +137,10 @@ constexpr int CLAIM_LEAD_KB = 64;
 // loader, MMA and 4 epilogue warps, and the odd CTA's forwarder, which
 // arrives once the odd CTA's readers (loader and 4 epilogue warps) have all
 // arrived on its tq_fwd.
-constexpr uint32_t TQ_READERS = 1 + 1 + 4 + 1;
-constexpr uint32_t TQ_ODD_READERS = 1 + 4;
+template <int NW>
+constexpr uint32_t TQ_READERS = 1 + 1 + Shape<NW>::EPI_WARPS + 1;
+template <int NW>
+constexpr uint32_t TQ_ODD_READERS = 1 + Shape<NW>::EPI_WARPS;
 
 constexpr uint32_t TMEM_COLS = 2 * BN;  // two 256-column accumulators, or one of 512
 constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, /*B MN-major*/ true);
@@ -571,21 +578,25 @@ __device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t
 
 // ------------------------------------------------------------------ epilogue
 
-// Warps 4-7 of both CTAs: this CTA's 128 rows of each pair tile.  Each
-// 64-column chunk goes TMEM -> registers -> bf16 -> swizzled staging rows ->
-// TMA store, with the next chunk's TMEM load in flight meanwhile and up to
-// EPI_BUFS stores still reading their staging buffers (chunks outside C are
-// read from TMEM and dropped).  With one accumulator
-// (NW = 2) the MMA waits for the whole read-out before the next tile, so the
-// accumulator is released as soon as its last chunk is in registers.
+// Epilogue warps 4 .. 4 + EPI_WARPS - 1 of both CTAs: this CTA's 128 rows of
+// each pair tile.  Warp w reads TMEM lanes 32 * (w % 4) .. + 31; with 8
+// warps (NW = 2) warps 4-7 take columns 0-255 and warps 8-11 columns 256-511.
+// Each 64-column chunk goes TMEM -> registers -> bf16 -> swizzled staging
+// rows -> TMA store, with the next chunk's TMEM load in flight meanwhile and
+// up to EPI_BUFS stores still reading their staging buffers (chunks outside C
+// are read from TMEM and dropped).  With one accumulator (NW = 2) the MMA
+// waits for the whole read-out before the next tile, so each warp releases
+// its part as soon as its last chunk is in registers.
 template <int NW>
 __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t tmem,
                              const ErrCtx& ec, int warp, uint32_t crank)
 {
     using S = Shape<NW>;
+    constexpr int CPW = S::CHUNKS / (S::EPI_WARPS / 4);  // chunks per warp and tile
     const uint32_t lane = lane_id();
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
-    uint8_t* buf0 = smem + S::OFF_EPI + quarter * S::EPI_BUFS * EPI_WARP_BYTES;
+    const int ch0 = ((warp - 4) >> 2) * CPW;  // this warp's first chunk of a tile
+    uint8_t* buf0 = smem + S::OFF_EPI + (warp - 4) * S::EPI_BUFS * EPI_WARP_BYTES;
     // the even CTA's tmem_empty[0], [1] (adjacent 8-byte barriers)
     const uint32_t empty_caddr0 = mapa_shared(smem_u32(&ctrl->tmem_empty[0]), 0);
     uint32_t acc = 0, aphase = 0, tq = 0, tqphase = 0, nstore = 0;
@@ -598,18 +609,20 @@ __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uin
         const int row0 = m0 + quarter * 32;
         if (!wait_bar(&ctrl->tmem_full[acc], aphase, ec, SITE_EPI_TMEM_FULL)) break;
         tc_fence_after();
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+        const uint32_t taddr =
+            tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN + ch0 * 64;
         uint32_t v0[32], v1[32];
         tmem_ld32(taddr, v0);
         tmem_ld32(taddr + 32, v1);
         tmem_ld_wait(v0);
         tmem_ld_wait(v1);
 #pragma unroll
-        for (int ch = 0; ch < S::CHUNKS; ++ch) {
+        for (int c = 0; c < CPW; ++c) {
+            const int ch = ch0 + c;
             uint32_t n0v[32], n1v[32];
-            if (ch + 1 < S::CHUNKS) {
-                tmem_ld32(taddr + (ch + 1) * 64, n0v);
-                tmem_ld32(taddr + (ch + 1) * 64 + 32, n1v);
+            if (c + 1 < CPW) {
+                tmem_ld32(taddr + (c + 1) * 64, n0v);
+                tmem_ld32(taddr + (c + 1) * 64 + 32, n1v);
             } else {
                 // accumulator fully read: the MMA may reuse it
                 tc_fence_before();
@@ -645,7 +658,7 @@ __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uin
                 }
                 __syncwarp();
             }
-            if (ch + 1 < S::CHUNKS) {
+            if (c + 1 < CPW) {
                 tmem_ld_wait(n0v);
                 tmem_ld_wait(n1v);
 #pragma unroll
@@ -896,7 +909,7 @@ __device__ void run_gather(const AgParams& p, uint8_t* buf0, uint64_t* gfull, in
 // ------------------------------------------------------------------ kernel
 
 template <int NW>
-__global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__ AgParams p)
+__global__ void __launch_bounds__(Shape<NW>::THREADS, 1) ag_gemm_kernel(const __grid_constant__ AgParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -913,14 +926,14 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctrl->tmem_full[i], 1);
-            mbar_init(&ctrl->tmem_empty[i], 2 * 4);  // 4 epilogue warps in each CTA
+            mbar_init(&ctrl->tmem_empty[i], 2 * Shape<NW>::EPI_WARPS);  // epilogue warps of both CTAs
         }
         for (int i = 0; i < GATHER_BUFS; ++i) mbar_init(&ctrl->gfull[i], 1);
         for (int i = 0; i < PROD_WARPS * PROD_BUFS; ++i) mbar_init(&ctrl->gprod[i], 1);
         for (int i = 0; i < TILE_Q; ++i) {
             mbar_init(&ctrl->tq_full[i], 1);
-            mbar_init(&ctrl->tq_empty[i], TQ_READERS);
-            mbar_init(&ctrl->tq_fwd[i], TQ_ODD_READERS);
+            mbar_init(&ctrl->tq_empty[i], TQ_READERS<NW>);
+            mbar_init(&ctrl->tq_fwd[i], TQ_ODD_READERS<NW>);
         }
         mbar_init(&ctrl->need_next, 1);
         mbar_init(&ctrl->mma_done, 1);
@@ -984,11 +997,12 @@ __global__ void __launch_bounds__(256, 1) ag_gemm_kernel(const __grid_constant__
     }
 }
 
-cudaLaunchConfig_t pair_config(unsigned pairs, cudaStream_t s, cudaLaunchAttribute* attr)
+cudaLaunchConfig_t pair_config(unsigned pairs, unsigned threads, cudaStream_t s,
+                               cudaLaunchAttribute* attr)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2u * pairs);
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = SMEM_ALLOC;
     cfg.stream = s;
     // Clusters of 2 only.  No cross-CTA wait depends on a CTA that has not
@@ -1034,12 +1048,14 @@ int ag_max_pairs()
     if (!set_smem_attr()) return 0;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = pair_config(static_cast<unsigned>(sms / 2), nullptr, attr);
-    // both widths use the same shared memory, threads and cluster shape
+    cudaLaunchAttribute attr1[1], attr2[1];
+    const unsigned pairs = static_cast<unsigned>(sms / 2);
+    const cudaLaunchConfig_t cfg1 = pair_config(pairs, Shape<1>::THREADS, nullptr, attr1);
+    const cudaLaunchConfig_t cfg2 = pair_config(pairs, Shape<2>::THREADS, nullptr, attr2);
+    // both widths use the same shared memory and cluster shape: one CTA per SM
     int n1 = 0, n2 = 0;
-    if (cudaOccupancyMaxActiveClusters(&n1, ag_gemm_kernel<1>, &cfg) != cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&n2, ag_gemm_kernel<2>, &cfg) != cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n1, ag_gemm_kernel<1>, &cfg1) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n2, ag_gemm_kernel<2>, &cfg2) != cudaSuccess)
         return 0;
     const int n = n1 < n2 ? n1 : n2;
     cached[dev] = n;
@@ -1050,9 +1066,11 @@ cudaError_t launch_ag_gemm(const AgParams& p, int pairs, cudaStream_t s)
 {
     if (!set_smem_attr()) return cudaErrorInvalidDevice;
     cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = pair_config(static_cast<unsigned>(pairs), s, attr);
-    return p.tile_n == 2 * BN ? cudaLaunchKernelEx(&cfg, ag_gemm_kernel<2>, p)
-                              : cudaLaunchKernelEx(&cfg, ag_gemm_kernel<1>, p);
+    const bool wide = p.tile_n == 2 * BN;
+    const cudaLaunchConfig_t cfg = pair_config(static_cast<unsigned>(pairs),
+                                               wide ? Shape<2>::THREADS : Shape<1>::THREADS, s, attr);
+    return wide ? cudaLaunchKernelEx(&cfg, ag_gemm_kernel<2>, p)
+                : cudaLaunchKernelEx(&cfg, ag_gemm_kernel<1>, p);
 }
 
 }  // namespace opw
