@@ -8,18 +8,21 @@
 // own rank's rows and rotate ("Threadblock Swizzling").
 //
 // CTAs work in pairs (clusters of 2) on 256 x 256 output tiles with one
-// tcgen05 cta_group::2 MMA: CTA c of the pair holds rows 128c..128c+127 of
-// the tile's A rows and columns 128c..128c+127 of B in its shared memory and
-// receives its 128 accumulator rows in its own TMEM.  8 warps per CTA (12
-// with 256 x 512 pair tiles):
+// tcgen05 cta_group::2 MMA per k step: CTA c of the pair holds rows
+// 128c..128c+127 of the tile's A rows and columns 128c..128c+127 of B in its
+// shared memory and receives its 128 accumulator rows in its own TMEM.  With
+// 256 x 512 pair tiles (below) each k step is two such MMAs, one per
+// 256-column half of the tile.  8 warps per CTA (12 with 256 x 512 tiles):
 //   warp 0     loader (both CTAs): takes tiles from the on-chip tile queue and
 //              TMA-loads this CTA's half of their A k-blocks (from the gathered
 //              buffer G, or in place from the local rank's own shard) and B
-//              k-blocks into a 6-stage ring; the bytes of both halves complete
-//              on the even CTA's `full` barrier.
+//              k-blocks into a 6-stage ring (3 stages of twice the B with
+//              256 x 512 tiles); the bytes of both halves complete on the
+//              even CTA's `full` barrier.
 //   warp 1     MMA (even CTA only): lane 0 alone issues the pair's
 //              tcgen05.mma (bf16 x bf16 -> fp32) into a double-buffered TMEM
-//              accumulator (2 x 128 lanes x 256 columns in each CTA).
+//              accumulator (2 x 128 lanes x 256 columns in each CTA; one
+//              128 lanes x 512 columns accumulator with 256 x 512 tiles).
 //   warp 2     gather producer (every CTA): claims flag tiles of A_r from a
 //              device counter in publish order, TMA-copies each into G through
 //              shared memory, waits for the copy to complete, and publishes the

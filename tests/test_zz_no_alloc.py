@@ -130,6 +130,23 @@ def test_matches_oracle_and_ag_gemm_on_two_calls_in_a_row(api):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("tile_n", [256, 512])
+def test_pair_tile_widths_match_oracle(api, tile_n):
+    """Both pair-tile widths through the no-allocation call, on a ragged N
+    (1288 = 2 x 512 + 264) with several wide tiles per pair, against the
+    oracle; the width is the one asked for."""
+    _gpu()
+    prob = AgProblem(inputs.ag_inputs(dict(R=4, M_r=384, K=448, N=1288, dist="normal", scale=0.5),
+                                      seed=59, slot_order=(3, 1, 0, 2)))
+    opts = api.make_opts(tile_n=tile_n, num_ctas=6)   # 3 pairs: several tiles each
+    assert api.ag_tile_n(4, 384, 1288, opts) == tile_n
+    status = torch.full((4,), -1, dtype=torch.int32, device="cuda")
+    st, G, C = _noalloc(api, prob, status, opts)
+    assert st[0] == api.OK, (tile_n, st)
+    _check_against_oracle(prob, G, C, f"tile_n {tile_n}")
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("mode", ["row_add", "checked", "checked_row_add"])
 def test_signal_modes_and_checked_publish(api, mode):
     """Batched row counters and the checked publish both need the shared
