@@ -147,6 +147,41 @@ def test_wide_tiles_many_per_pair(api):
     assert np.array_equal(host_bits(p1.C), host_bits(p2.C))
 
 
+@pytest.mark.parametrize("mode", ["serial", "checked", "swizzle", "no_local", "row_add", "skew"])
+def test_wide_tiles_in_every_mode(api, mode):
+    """256 x 512 pair tiles under each synchronisation, signal and schedule
+    option, over 2 epochs: G bit for bit and C against the oracle, the flags
+    (or row counters) at their epoch values, and C bit for bit against the
+    same option on 256 x 256 tiles."""
+    R, M_r, K, N = 4, 256, 384, 1288
+    d = inputs.ag_inputs(_cfg(R, M_r, K, N), seed=80 + len(mode))
+    kw = {"serial": dict(sync_mode=api.SYNC_SERIAL), "checked": dict(sync_mode=api.SYNC_CHECKED),
+          "swizzle": dict(schedule=api.SCHED_SWIZZLE), "no_local": dict(local_rank=-1),
+          "row_add": dict(signal_mode=api.SIGNAL_ROW_ADD),
+          "skew": dict(publish_perm=(2, 0, 3, 1), delay_ns=(0, 20000, 5000, 0))}[mode]
+    ft = api.ag_flag_tile(M_r, K)
+    row_add = mode == "row_add"
+    n_slots = api.ag_num_row_counters(R, M_r, K) if row_add else api.ag_num_flags(R, M_r, K)
+    out = {}
+    for tile_n in (512, 256):
+        prob = AgProblem(d)
+        sig = api.Signal(n_slots)
+        opts = api.make_opts(tile_n=tile_n, num_ctas=6, **kw)
+        for _ in range(2):
+            e = sig.next_epoch()
+            prob.run(api, sig, e, opts)
+            assert sig.status()[0] == api.OK, (mode, tile_n)
+            want = (oracle.expected_row_counters(n_slots, e, K // ft) if row_add
+                    else oracle.expected_flags(n_slots, e))
+            assert np.array_equal(sig.flags().cpu().numpy(), want), (mode, tile_n, e)
+        sig.close()
+        out[tile_n] = prob
+    G_ref, C_ref = out[512].oracle_full()
+    assert np.array_equal(host_bits(out[512].G), G_ref)
+    assert_gemm_close(host_bits(out[512].C), C_ref, what=f"{mode}: C")
+    assert np.array_equal(host_bits(out[512].C), host_bits(out[256].C))
+
+
 def test_tile_width_choice(api):
     """The library's width for the benchmark layers on the full grid follows
     its documented rule: 512 when whole waves of wide tiles, at 1.93 times a
