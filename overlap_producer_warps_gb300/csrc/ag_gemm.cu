@@ -137,9 +137,9 @@ static_assert(OFF_GATHER % 1024 == 0, "swizzled buffers must be 1024-byte aligne
 constexpr int CLAIM_LEAD_KB = 64;
 
 // Arrivals that free a tile-queue slot on the even CTA's tq_empty: its
-// loader, MMA and 4 epilogue warps, and the odd CTA's forwarder, which
-// arrives once the odd CTA's readers (loader and 4 epilogue warps) have all
-// arrived on its tq_fwd.
+// loader, MMA and epilogue warps (4, or 8 with 256 x 512 tiles), and the odd
+// CTA's forwarder, which arrives once the odd CTA's readers (loader and
+// epilogue warps) have all arrived on its tq_fwd.
 template <int NW>
 constexpr uint32_t TQ_READERS = 1 + 1 + Shape<NW>::EPI_WARPS + 1;
 template <int NW>
