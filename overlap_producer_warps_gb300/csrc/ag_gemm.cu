@@ -16,7 +16,7 @@
 //   warp 0     loader (both CTAs): takes tiles from the on-chip tile queue and
 //              TMA-loads this CTA's half of their A k-blocks (from the gathered
 //              buffer G, or in place from the local rank's own shard) and B
-//              k-blocks into a 6-stage ring (3 stages of twice the B with
+//              k-blocks into a 6-stage ring (4 stages of twice the B with
 //              256 x 512 tiles); the bytes of both halves complete on the
 //              even CTA's `full` barrier.
 //   warp 1     MMA (even CTA only): lane 0 alone issues the pair's
@@ -68,9 +68,10 @@ constexpr int B_HALF_BYTES = BK * HALF_N * 2;   // 16 KiB: 2 chunks of 64 column
 //           buffers it fits the budget (225 KiB); against 5 stages with 4
 //           buffers it was 1.3-2.2 % faster fused in a burst.
 //   NW = 2: two N = 256 MMAs per k step (B columns 0-255 and 256-511 of the
-//           tile) into one 512-column accumulator; a 3-stage ring of 48 KiB
-//           stages (3 x 1024 cycles of MMA in flight, as much as the 6 narrow
-//           stages).  The MMA waits for the read-out of the accumulator, so
+//           tile) into one 512-column accumulator; a 4-stage ring of 48 KiB
+//           stages (against 3 stages, whose loads often landed after the MMA
+//           needed them, 1-2 % faster in a burst).  The MMA waits for the
+//           read-out of the accumulator, so
 //           8 epilogue warps (384 threads) read its two column halves at once
 //           into registers and release it before they store: about 1.8k
 //           cycles per tile against 5.2k when the stores came first.  A CTA
@@ -82,14 +83,18 @@ constexpr int B_HALF_BYTES = BK * HALF_N * 2;   // 16 KiB: 2 chunks of 64 column
 // The host picks the width per launch (opts.tile_n, or from the wave counts).
 template <int NW>
 struct Shape {
-    static constexpr int STAGES = NW == 1 ? 6 : 3;
+    static constexpr int STAGES = NW == 1 ? 6 : 4;
     static constexpr int B_STAGE = NW * B_HALF_BYTES;   // this CTA's B bytes per stage
     static constexpr int OFF_B = STAGES * A_STAGE_BYTES;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;  // the ring ends here
     static constexpr int EPI_WARPS = 4 * NW;             // warps 4 .. 4 + EPI_WARPS - 1
     static constexpr int THREADS = 32 * (4 + EPI_WARPS);
-    static constexpr int EPI_BUFS = NW == 1 ? 1 : 2;    // staging buffers per epilogue warp
-    static constexpr int EPI_END = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_WARP_BYTES;
+    // one staging buffer per epilogue warp: 32 rows x 64 columns (128B swizzle),
+    // or x 32 columns (64B swizzle) with 256 x 512 tiles, whose stores come
+    // after the accumulator is released and so can be smaller and serial
+    static constexpr int EPI_COLS = NW == 1 ? 64 : 32;
+    static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;
+    static constexpr int EPI_END = OFF_EPI + EPI_WARPS * EPI_BUF_BYTES;
     static constexpr uint32_t TX = 2u * (A_STAGE_BYTES + B_STAGE);  // both CTAs' bytes per stage
     static constexpr int ACCS = NW == 1 ? 2 : 1;        // TMEM accumulators
     static constexpr int CHUNKS = NW * BN / 64;         // 64-column epilogue chunks per tile
@@ -583,35 +588,25 @@ __device__ void run_mma(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t
 
 // ------------------------------------------------------------------ epilogue
 
-// Epilogue warps 4 .. 4 + EPI_WARPS - 1 of both CTAs: this CTA's 128 rows of
-// each pair tile.  Warp w reads TMEM lanes 32 * (w % 4) .. + 31; with 8
-// warps (NW = 2) warps 4-7 take columns 0-255 and warps 8-11 columns 256-511.
-// Each 64-column chunk goes TMEM -> registers -> bf16 -> swizzled staging
-// rows -> TMA store, with the next chunk's TMEM load in flight meanwhile and
-// up to EPI_BUFS stores still reading their staging buffers (chunks outside C
-// are read from TMEM and dropped).  With one accumulator (NW = 2) the MMA
-// waits for the whole read-out before the next tile, so each warp reads its
-// whole part into registers and releases it before storing anything.
-// One warp stores 32 rows x 64 columns of C (w: this lane's row as 32 packed
-// bf16 pairs) through the next of its `nbufs` staging buffers: swizzled
-// st.shared, then one TMA store in a bulk group of its own.  The store that
-// last used the buffer is nbufs groups back and must have finished reading it.
-template <int NBUFS>
-__device__ __forceinline__ void store_chunk(const AgParams& p, uint8_t* buf0, uint32_t& nstore,
-                                            const uint32_t (&w)[32], int x, int row0)
+// One warp stores 32 rows x COLS columns of C (w: this lane's row as COLS / 2
+// packed bf16 pairs) through its staging buffer: swizzled st.shared, then one
+// TMA store in a bulk group of its own, once the previous store has finished
+// reading the buffer.  The C tensor map's box and swizzle match COLS: 64
+// columns with the 128-byte swizzle (16-byte chunk j of row r at j ^ (r & 7)),
+// 32 columns with the 64-byte swizzle (at j ^ ((r >> 1) & 3)).
+template <int COLS>
+__device__ __forceinline__ void store_chunk(const AgParams& p, uint8_t* buf, const uint32_t* w,
+                                            int x, int row0)
 {
     const uint32_t lane = lane_id();
-    uint8_t* buf = buf0 + (nstore % NBUFS) * EPI_WARP_BYTES;
-    ++nstore;
-    const uint32_t row_addr = smem_u32(buf) + lane * 128u;
-    if (lane == 0) bulk_wait_read<NBUFS - 1>();
+    const uint32_t row_addr = smem_u32(buf) + lane * (COLS * 2u);
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
-    // row `lane`, 16-byte chunk j stored at chunk j ^ (row & 7): the 128-byte
-    // swizzle the C tensor map expects
+    const uint32_t sw = COLS == 64 ? (lane & 7u) : ((lane >> 1) & 3u);
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-        st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), w[4 * j],
-                     w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    for (int j = 0; j < COLS / 8; ++j)
+        st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ sw) << 4), w[4 * j], w[4 * j + 1],
+                     w[4 * j + 2], w[4 * j + 3]);
     fence_async_shared();
     __syncwarp();
     if (lane == 0) {
@@ -621,6 +616,15 @@ __device__ __forceinline__ void store_chunk(const AgParams& p, uint8_t* buf0, ui
     __syncwarp();
 }
 
+// Epilogue warps 4 .. 4 + EPI_WARPS - 1 of both CTAs: this CTA's 128 rows of
+// each pair tile.  Warp w reads TMEM lanes 32 * (w % 4) .. + 31; with 8
+// warps (NW = 2) warps 4-7 take columns 0-255 and warps 8-11 columns 256-511.
+// NW = 1: each 64-column chunk goes TMEM -> registers -> bf16 -> swizzled
+// staging rows -> TMA store, with the next chunk's TMEM load in flight
+// meanwhile (chunks outside C are read from TMEM and dropped); the other
+// accumulator keeps the MMA busy.  NW = 2: the one accumulator holds up the
+// next tile's MMAs until it is read, so each warp reads its whole part into
+// registers, releases it, and then stores it 32 columns at a time.
 template <int NW>
 __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uint32_t tmem,
                              const ErrCtx& ec, int warp, uint32_t crank)
@@ -630,10 +634,10 @@ __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uin
     const uint32_t lane = lane_id();
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
     const int ch0 = ((warp - 4) >> 2) * CPW;  // this warp's first chunk of a tile
-    uint8_t* buf0 = smem + S::OFF_EPI + (warp - 4) * S::EPI_BUFS * EPI_WARP_BYTES;
+    uint8_t* buf = smem + S::OFF_EPI + (warp - 4) * S::EPI_BUF_BYTES;
     // the even CTA's tmem_empty[0], [1] (adjacent 8-byte barriers)
     const uint32_t empty_caddr0 = mapa_shared(smem_u32(&ctrl->tmem_empty[0]), 0);
-    uint32_t acc = 0, aphase = 0, tq = 0, tqphase = 0, nstore = 0;
+    uint32_t acc = 0, aphase = 0, tq = 0, tqphase = 0;
     while (true) {
         const int q = pop_tile(ctrl, ec, tq, tqphase, crank);
         if (q < 0) break;
@@ -667,8 +671,12 @@ __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uin
             if (lane == 0) mbar_arrive_cluster(empty_caddr0 + 8u * acc);
 #pragma unroll
             for (int c = 0; c < CPW; ++c)
-                if (row0 < p.M && n0 + (ch0 + c) * 64 < p.N)  // the same for the whole warp
-                    store_chunk<S::EPI_BUFS>(p, buf0, nstore, pk[c], n0 + (ch0 + c) * 64, row0);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int x = n0 + (ch0 + c) * 64 + h * 32;
+                    if (row0 < p.M && x < p.N)  // the same for the whole warp
+                        store_chunk<S::EPI_COLS>(p, buf, &pk[c][16 * h], x, row0);
+                }
             if (++acc == S::ACCS) { acc = 0; aphase ^= 1u; }
             continue;
         }
@@ -697,7 +705,7 @@ __device__ void run_epilogue(const AgParams& p, uint8_t* smem, AgCtrl* ctrl, uin
                     w[i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
                     w[16 + i] = pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
                 }
-                store_chunk<S::EPI_BUFS>(p, buf0, nstore, w, n0 + ch * 64, row0);
+                store_chunk<S::EPI_COLS>(p, buf, w, n0 + ch * 64, row0);
             }
             if (c + 1 < CPW) {
                 tmem_ld_wait(n0v);

@@ -215,7 +215,8 @@ opw_status ag_fill_params(const opw_symm* symm, size_t a_off, int64_t M_r, int64
                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&p.g_load, G_dev, K, M, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&p.b_load, B_dev, N, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&p.c_store, C_dev, N, M, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map(&p.c_store, C_dev, N, M, tile_n == 2 * BN ? 32 : 64, 32,
+                  tile_n == 2 * BN ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
         return OPW_ERR_CUDA;
     p.local_rank = o.local_rank;
     if (o.local_rank >= 0 &&

@@ -55,7 +55,8 @@ struct AgParams {
     CUtensorMap g_store;               // G [M, K], box {ft, 32}, no swizzle (producer store)
     CUtensorMap g_load;                // G [M, K], box {64, 128}, 128B swizzle (consumer A)
     CUtensorMap b_load;                // B [K, N], box {64, 64}, 128B swizzle (consumer B)
-    CUtensorMap c_store;               // C [M, N], box {64, 32}, 128B swizzle (epilogue)
+    CUtensorMap c_store;               // C [M, N], box {64, 32}, 128B swizzle (epilogue);
+                                       // {32, 32}, 64B swizzle with 256 x 512 tiles
     CUtensorMap a_local_load;          // A_local [M_r, K], box {64, 128}, 128B swizzle (consumer A)
     int64_t* flags;
     int32_t* status;
