@@ -71,15 +71,14 @@ constexpr int B_HALF_BYTES = BK * HALF_N * 2;   // 16 KiB: 2 chunks of 64 column
 //           tile) into one 512-column accumulator; a 4-stage ring of 48 KiB
 //           stages (against 3 stages, whose loads often landed after the MMA
 //           needed them, 1-2 % faster in a burst).  The MMA waits for the
-//           read-out of the accumulator, so
-//           8 epilogue warps (384 threads) read its two column halves at once
-//           into registers and release it before they store: about 1.8k
-//           cycles per tile against 5.2k when the stores came first.  A CTA
-//           reads a
-//           quarter less operand data from L2 per FLOP.  In a probe GEMM with
-//           random operands and whole waves it ran 3.7 % faster in a burst and
-//           5-8 % faster under the power cap, where the lower on-chip traffic
-//           bought a 9 % higher SM clock.
+//           read-out of the accumulator, so 8 epilogue warps (384 threads)
+//           read its two column halves at once into registers and release it
+//           before they store: about 1.8k cycles per tile against 5.2k when
+//           the stores came first.  A CTA reads a quarter less operand data
+//           from L2 per FLOP.  In a probe GEMM with random operands and whole
+//           waves it ran 3.7 % faster in a burst and 5-8 % faster under the
+//           power cap, where the lower on-chip traffic bought a 9 % higher SM
+//           clock.
 // The host picks the width per launch (opts.tile_n, or from the wave counts).
 template <int NW>
 struct Shape {
