@@ -340,7 +340,10 @@ opw_status opw_ag_gemm(const opw_symm* symm, size_t a_off, int64_t M_r, int64_t 
  *
  * Set-up: the first call on a device, with that device current, looks up
  * the array's device address and keeps it for the life of the process.  Make
- * that first call before any stream capture.  cudaDeviceReset() (or anything
+ * that first call before any stream capture.  After it, a call can be
+ * captured in a CUDA graph: it launches the same two kernels (clear, then
+ * AG-GEMM) with the same arguments every time, so replaying the graph
+ * recomputes G and C from whatever the captured buffers then hold.  cudaDeviceReset() (or anything
  * else that destroys the device's primary context) invalidates the kept
  * address: do not call this entry point on that device afterwards.
  *
