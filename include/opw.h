@@ -72,7 +72,8 @@ int32_t opw_abi_version(void);
  * (SignalOp SET, "Distributed Architecture Design" 2.3); a waiter spins until
  * flag >= epoch (the GE predicate of section 6.3).  Waiting never modifies a
  * flag (non-consuming wait, section 6.3); only opw_signal_reset() writes
- * flags back to 0 ("the constraint falls on the reset side").  Flags are
+ * flags back to 0, so the reset is the one step that must be ordered against
+ * the launches (section 6.3).  Flags are
  * dense (8 bytes apart): on GB300 the L2 is the coherence point for
  * .gpu-scope release/acquire, so the 64-byte slot stride that section 4.2
  * needs on Ascend buys nothing here.
@@ -139,8 +140,9 @@ typedef struct {
 
 #define OPW_SYNC_OVERLAP 0   /* per-tile flags: consumers start as tiles land */
 #define OPW_SYNC_SERIAL  1   /* consumers wait until EVERY tile is published
-                                (the "test with barrier sync first" debug mode
-                                of "Triton-distributed Semantics", Best Practices 8) */
+                                (the debugging step of "Triton-distributed
+                                Semantics", Best Practices 8: rule out the
+                                fine-grained synchronisation first) */
 #define OPW_SYNC_CHECKED 2   /* as OVERLAP, but every publish is an atomic exchange
                                 that must find epoch-1 in the slot (with
                                 OPW_SIGNAL_ROW_ADD: a fetch-add that must find a
@@ -178,8 +180,9 @@ typedef struct {
                                   (SignalOp ADD, "Distributed Architecture Design"
                                   2.3); a consumer starts on the row only when the
                                   counter reaches epoch * K/ft, i.e. every k-tile of
-                                  the row is in ("Batch Signals When Possible",
-                                  Best Practices 4).  Counters are cumulative, so a
+                                  the row is in (signals shared by tiles that are
+                                  always used together, Best Practices 4).
+                                  Counters are cumulative, so a
                                   signal object must keep one mode and one K/ft
                                   between resets. */
 
@@ -265,8 +268,8 @@ int64_t opw_ag_trace_words(int32_t R, int64_t M_r, int64_t N, int64_t K);
  * on-chip power draw, so a higher clock under the power cap), but holds its
  * one 512-column TMEM accumulator through the epilogue; the library takes it
  * when its whole waves of tiles, at 1.93 times the time of a 256-wide wave,
- * are shorter than the 256-wide waves.  This is a refinement of the pages'
- * "one program per output tile" ("AllGather and GEMM Overlapping"), with no
+ * are shorter than the 256-wide waves.  This refines the pages' consumer
+ * program, which owns one output tile ("AllGather and GEMM Overlapping"), with no
  * change to the results: every output element sums the same products in the
  * same order.  Returns 256, 512, or -1 (invalid arguments, or no CUDA device
  * to size the grid for when opts->tile_n is 0).  opts may be NULL.

@@ -15,8 +15,9 @@
  *   - same page, section "GEMM and ReduceScatter Overlapping": per-rank GEMM
  *     partials are reduced and each row block is scattered to its rank.
  *     Result: S = sum_r A_r * B_r, out_j = rows of block j of S.
- *   - "Distributed Architecture Design", section 5.3 "Remote Address
- *     Resolution of symm_at": remote = ptr - heap_base[self] + heap_base[pe].
+ *   - "Distributed Architecture Design", section 5.3 (remote addresses of
+ *     symm_at): an address in the own slice moves to rank pe's slice by
+ *     subtracting the own slice's base and adding rank pe's.
  *   - "Triton-distributed Semantics", section "Threadblock Swizzling": the row
  *     tile index is rotated by rank * tiles_per_pe modulo the tile count.
  *

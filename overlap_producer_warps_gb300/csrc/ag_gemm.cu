@@ -174,8 +174,8 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, const 
 }
 
 // Pair tile at position `pos` of the consumers' tile order, which both
-// schedules share ("Threadblock Swizzling": the PE starts on its own rows;
-// "by the time a PE needs remote data, it's likely already transferred").
+// schedules share ("Threadblock Swizzling": a PE begins with its own rows, and
+// the remote rows have usually arrived by the time it reaches them).
 // Pair rows are taken in groups of p.group_rows; within a group the column
 // index runs slowest, so when B is larger than L2 can hold next to
 // everything else, the pairs working at the same time share B column tiles

@@ -26,7 +26,7 @@
 //   warp 2      allocates / frees the pair's TMEM.
 //   warp 3      the receiving side, when the caller asks for it (recv != NULL):
 //               for each pair tile it acquires the flags of the OTHER CTA's
-//               rows ("consumer waits for tiles", step 3) and copies each
+//               rows (step 3: it waits until a tile is ready) and copies each
 //               finished 128x128 tile from its rank's block into recv.  The
 //               other CTA runs on another SM, so every copy reads data that a
 //               different SM's TMA stores wrote and released.  Otherwise idle.

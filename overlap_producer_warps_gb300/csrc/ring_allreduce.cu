@@ -9,7 +9,8 @@
 // steps, guarded by one flag per (receiving rank, step, piece) that holds the
 // epoch once the piece has landed in that rank's receive slot.  So a piece of
 // step s+1 starts as soon as the same piece of step s has arrived, with no
-// barrier across ranks ("Each tile is independently synchronized").
+// barrier across ranks: every tile has its own wait and notify ("Example:
+// Ring AllReduce with Overlap").
 //
 // On one GPU the "send" is a store into the next rank's receive slot (its
 // slice of the heap) and the "notify" a st.release.gpu of that slot's flag.
