@@ -15,7 +15,7 @@ function cites the passage of the pages it follows:
   AllReduce with Overlap".
 * Aboleth README -- Tier-2 all-to-all (put, signal with epoch, wait).
 * "Distributed Architecture Design" -- section 2.3 (SignalOp SET and ADD) and
-  section 5.3 (remote address resolution of symm_at).
+  section 5.3 (how symm_at finds a remote address).
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 against brute force on tiny inputs, closed forms, library routines on special
