@@ -338,7 +338,7 @@ void opw_oracle_expected_flags(int64_t n_slots, int64_t epoch, int64_t* out)
 
 /*
  * Batched signals with SignalOp ADD ("Distributed Architecture Design", 2.3:
- * ADD adds the given value to the current signal value; "Triton-distributed
+ * an ADD increments the signal by its operand; "Triton-distributed
  * Semantics", Best Practices 4: tiles that are always consumed together may
  * share one signal).  One counter per row of flag tiles; every launch adds 1
  * for each of the row's T_k k-tiles, starting from 0 after a reset.  After
