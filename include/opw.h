@@ -93,6 +93,14 @@ opw_status opw_signal_alloc(opw_signal** out, int64_t num_slots, void* stream);
  * internal counters := 0; and set the host epoch counter to 0, so the next
  * epoch is 1.  The caller must not have launches on this object in flight
  * on other streams.  Errors: INVALID_ARG (NULL), CUDA.
+ *
+ * CUDA graphs: a launch takes its epoch and claim bases from the host, so a
+ * captured launch replays the same ones.  Capture this reset and then the
+ * launch at epoch 1 (after one call outside any capture, which sets up the
+ * library's per-device state): every replay zeroes the flags and publishes
+ * epoch 1 again.  A whole tensor-parallel step (opw_ag_gemm, then
+ * opw_gemm_rs, each behind the reset of its own signal object) replays
+ * this way.
  */
 opw_status opw_signal_reset(opw_signal* sig, void* stream);
 
