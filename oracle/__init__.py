@@ -31,8 +31,12 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "opw_oracle.c")
-_BUILD_DIR = os.path.join(_HERE, "_build")
+# The test of the pins themselves (tests/test_oracle_mutations.py) plants one
+# mistake in a copy of the C source and names the copy in OPW_ORACLE_SRC; the
+# library is then built next to that copy, never over the real one.
+_SRC = os.environ.get("OPW_ORACLE_SRC") or os.path.join(_HERE, "opw_oracle.c")
+_BUILD_DIR = (os.path.join(os.path.dirname(os.path.abspath(_SRC)), "_build")
+              if os.environ.get("OPW_ORACLE_SRC") else os.path.join(_HERE, "_build"))
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 _lock = threading.Lock()
 _lib = None

@@ -73,6 +73,26 @@ def test_bf16_encode_is_nearest_with_ties_to_even():
     assert np.all((enc[tie] & 1) == 0)
 
 
+def test_bf16_encode_special_values_match_torch():
+    # Infinities and signed zeros bit for bit against torch's binary32 -> bf16
+    # cast; every NaN (any sign or payload) to a NaN, whose payload neither
+    # side fixes (torch gives 0xffff here).  Plus fp64 values beyond binary32's
+    # range, which overflow to infinity or flush to a signed zero.
+    special = np.array([0x7F800000, 0xFF800000, 0x00000000, 0x80000000, 0x7FC00000, 0xFFC00000,
+                        0x7F800001, 0xFF812345, 0x7FFFFFFF], dtype=np.uint32).view(np.float32)
+    ours = oracle.f64_to_bf16(special.astype(np.float64))
+    ref = torch.from_numpy(special).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(special)
+
+    def is_nan_bits(b):
+        return ((b & 0x7F80) == 0x7F80) & ((b & 0x007F) != 0)
+    assert np.all(is_nan_bits(ours[nan])) and np.all(is_nan_bits(ref[nan]))
+    assert np.array_equal(ours[~nan], ref[~nan])
+    big = np.array([1e300, -1e300, 2.0 ** 128, -(2.0 ** 129), 1e-300, -1e-300])
+    assert [hex(v) for v in oracle.f64_to_bf16(big)] == ["0x7f80", "0xff80", "0x7f80", "0xff80",
+                                                        "0x0", "0x8000"]
+
+
 # ---------------------------------------------------------------- symm_at
 
 def test_symm_at_golden(golden):
