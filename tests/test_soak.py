@@ -150,3 +150,52 @@ def test_gemm_rs_grids_repeat_bit_for_bit(api):
     assert int(flag_bad) == 0, f"{int(flag_bad)} flags not at their launch's epoch"
     assert int(bad) == 0, f"{int(bad)} output elements differ from the first launch"
     sig.close()
+
+
+@pytest.mark.parametrize("name,launches", [("ag_tp", 40), ("ag_skew", 12), ("rs_tp", 30)])
+def test_full_size_layers_repeat_bit_for_bit(api, name, launches):
+    """The benchmark's layers at full size, in its launch configuration (the
+    skew layer with its permuted publish order and delays): every launch
+    reproduces the first one's bits.  Parity of that first result with the
+    oracle at these sizes is the full-size parity tests' part."""
+    cfg = inputs.CONFIGS[name]
+    if name.startswith("rs"):
+        d = inputs.rs_inputs(cfg, seed=0)
+        prob = RsProblem(d)
+        sig = api.Signal(api.rs_num_flags(prob.R, prob.M, prob.N))
+        outs = [prob.heap[int(prob.rank_off[j]) + d["out_off"]:
+                          int(prob.rank_off[j]) + d["out_off"] + prob.Mb * prob.N * 2]
+                for j in range(prob.R)]
+        opts = None
+    else:
+        d = inputs.ag_inputs(cfg, seed=0)
+        prob = AgProblem(d)
+        sig = api.Signal(api.ag_num_flags(prob.R, prob.M_r, prob.K))
+        outs = [prob.G.view(torch.uint8).reshape(-1), prob.C.view(torch.uint8).reshape(-1)]
+        opts = None
+        if cfg.get("skew"):
+            perm, delay = inputs.skew_schedule(0, prob.R)
+            opts = api.make_opts(publish_perm=perm, delay_ns=delay)
+    first = None
+    bad = torch.zeros((), dtype=torch.int64, device="cuda")
+    flag_bad = torch.zeros((), dtype=torch.int64, device="cuda")
+    for i in range(launches):
+        for t in outs:
+            t.fill_(255)
+        e = sig.next_epoch()
+        prob.run(api, sig, e, opts)
+        flag_bad += (sig.flags() != e).sum()
+        if first is None:
+            first = [t.clone() for t in outs]
+            continue
+        for t, f in zip(outs, first):
+            bad += (t != f).sum()
+    torch.cuda.synchronize()
+    assert sig.status()[0] == api.OK
+    assert int(flag_bad) == 0, f"{int(flag_bad)} flags not at their launch's epoch"
+    assert int(bad) == 0, f"{int(bad)} output bytes differ from the first launch"
+    # the first launch wrote every output byte (none kept the 0xff pattern of a
+    # bf16 NaN: the inputs are finite)
+    for f in first:
+        assert not bool((f.view(torch.int16) == -1).any())
+    sig.close()
