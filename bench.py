@@ -234,6 +234,63 @@ def oracle_sample(d, min_seconds=10.0, max_seconds=30.0):
                       f"K={d['K']}), fp64, {el:.1f} s"}
 
 
+def oracle_rows_results(seconds=2.0):
+    """The oracle timed beside each per-configuration row, on the host cores
+    (part of the CPU-baseline leg): random output rows of the GEMM layers for
+    about `seconds` each, in TFLOP/s, and one whole call of the ring AllReduce
+    and of the all-to-all on the same workloads as their GPU rows, in the same
+    GB/s of algorithmic bytes."""
+    import oracle
+    from overlap_producer_warps_gb300 import inputs
+    oracle.build()
+    cores = oracle.threads()
+    chunk = max(4, cores)
+    rng = np.random.default_rng(11)
+    out = {"cores": cores, "kind": "oracle"}
+
+    def timed(step, unit_work):
+        work, n, t0 = 0.0, 0, time.perf_counter()
+        while True:
+            step()
+            work += unit_work
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return work / el, n, el
+
+    for name in ("ag_tp", "ag_mlp"):
+        d = inputs.ag_inputs(inputs.CONFIGS[name], seed=0)
+        M = d["R"] * d["M_r"]
+        rate, n, el = timed(lambda: oracle.ag_gemm_rows(
+            d["heap"], d["rank_off"], d["R"], d["a_off"], d["M_r"], d["N"], d["K"], d["B"],
+            rng.integers(0, M, size=chunk)), 2.0 * chunk * d["N"] * d["K"])
+        out[name] = {"tflops": rate / 1e12, "sample": f"{n * chunk} random rows of C, {el:.1f} s"}
+    d = inputs.rs_inputs(inputs.CONFIGS["rs_tp"], seed=0)
+    rate, n, el = timed(lambda: oracle.gemm_rs_rows(
+        d["heap"], d["rank_off"], d["R"], d["a_off"], d["b_off"], d["M"], d["N"], d["K_r"],
+        rng.integers(0, d["M"], size=chunk)), 2.0 * chunk * d["N"] * d["K_r"] * d["R"])
+    out["rs_tp"] = {"tflops": rate / 1e12, "sample": f"{n * chunk} random rows of S, {el:.1f} s"}
+
+    R, n = 8, 8 * (1 << 21)   # the ring row's workload
+    d = inputs.ring_inputs(R, n, seed=0)
+    chunk_b = (n // R) * 4
+    algo = R * chunk_b * (2 + 3 * (R - 2) + 4 + 3 * (R - 2) + 2)
+    t0 = time.perf_counter()
+    oracle.ring_allreduce(d["heap"], d["rank_off"], R, d["data_off"], d["out_off"], n)
+    el = time.perf_counter() - t0
+    out["ring_allreduce"] = {"ms": el * 1e3, "hbm_gbs": algo / el / 1e9,
+                             "sample": "one whole call (8 ranks x 64 MiB, binary32, one thread)"}
+    del d
+    B = 8 << 20   # the all-to-all row's workload
+    d = inputs.alltoall_inputs(R, B, seed=0)
+    t0 = time.perf_counter()
+    oracle.alltoall(d["heap"], d["rank_off"], R, d["send_off"], d["recv_off"], B)
+    el = time.perf_counter() - t0
+    out["alltoall"] = {"ms": el * 1e3, "hbm_gbs": 2 * R * R * B / el / 1e9,
+                       "sample": "one whole call (8 ranks x 8 MiB slices, one thread)"}
+    return out
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args, rank, world):
@@ -912,6 +969,8 @@ def run_ours(args, rank, world, dist):
         line["per_config"]["clocks"] = sampler2.summary()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(d, min_seconds=args.cpu_seconds)
+        if not args.no_extra:
+            line["cpu_baseline"]["rows"] = oracle_rows_results()
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
